@@ -1,0 +1,655 @@
+#!/usr/bin/env python3
+"""Benchmark: all-reduce HBM GB/s over N virtual ranks on one GB300.
+
+One step is one pass of the whole hot path over one batch of synthetic
+input resident in HBM:
+
+* the gradient bucket: n = 8 virtual ranks, float32, 25,000,000 elements
+  (100 MB) per rank, normal(0, 1e-2):
+  ring all-reduce, one-shot all-reduce, two-shot all-reduce,
+  ring reduce-scatter, direct reduce-scatter (input = the bucket),
+  ring all-gather, direct all-gather (input = 3,125,000-element shards);
+* the LL / LL128 payloads: 4 sources of 256 MiB int32 in [-2^20, 2^20],
+  flag = step counter: 4 packs and one 4-source unpack-reduce per format.
+
+value = floor bytes of the step (every input read once, every output
+written once, per operation) / device time of the step, in GB/s.  Inputs
+(800 MB per all-reduce, 1 GiB of LL payload) are larger than the 129 MB L2,
+so no flush is needed between operations.
+
+--impl reference times the CPU oracle on a bounded sample of the same step.
+--sweep FILE writes the message-size sweep (1 KiB .. 1 GiB per rank,
+n = 2, 4, 8, int32 and bfloat16, every schedule) as JSON lines and a
+tuning table for the selector.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "allreduce HBM GB/s (% of 8 TB/s) & busbw vs msg size, N virtual ranks, 1 GB300"
+UNIT = "GB/s"
+N_RANKS = 8
+BUCKET = 25_000_000
+LL_SRC = 4
+LL_BYTES = 256 << 20
+WORKLOAD = ("gradient bucket n=8 fp32 25M/rank (ring, one-shot, two-shot AR; ring+direct RS, AG) "
+            "+ LL/LL128 pack + 4-source unpack-reduce of 256 MiB int32")
+HBM_NOMINAL = 8000.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------
+# clocks (nvidia-smi sampled during the timed region)
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 7:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx = float(p[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, p[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# the step
+# --------------------------------------------------------------------------
+def floor_bytes(op, n, S, e=4):
+    """Bytes a call must move at least: every input read once, every output
+    written once (S = per-rank message bytes as the op defines it)."""
+    if op.startswith("ar_"):
+        return 2 * n * S
+    if op.startswith("rs_"):  # S = per-rank input (n * recvcount elements)
+        return n * S + S
+    if op.startswith("ag_"):  # S = per-rank output (n * sendcount elements)
+        return S + n * S
+    raise ValueError(op)
+
+
+def bus_factor(op, n):
+    return 2 * (n - 1) / n if op.startswith("ar_") else (n - 1) / n
+
+
+class Step:
+    """Device buffers and the sequence of C-ABI calls of one step."""
+
+    def __init__(self, torch, rra, inputs, seed, scale=1):
+        self.torch, self.rra = torch, rra
+        n = N_RANKS
+        self.count = BUCKET // scale
+        self.rc = self.count // n
+        self.llb = LL_BYTES // scale
+        dev = torch.device("cuda", torch.cuda.current_device())
+        xs = inputs.cfg_gradient_bucket(self.count, seed=seed)
+        shards = [x[: self.rc].copy() for x in xs]
+        ps = inputs.cfg_ll_payloads(self.llb, LL_SRC, seed=seed)
+        self.host = {"bucket": xs, "shards": shards, "payloads": ps}
+        self.x = [torch.from_numpy(x).to(dev) for x in xs]
+        self.sh = [torch.from_numpy(x).to(dev) for x in shards]
+        self.pl = [torch.from_numpy(p).to(dev) for p in ps]
+        self.ar_out = [torch.empty_like(t) for t in self.x]
+        self.rs_out = [torch.empty(self.rc, dtype=torch.float32, device=dev) for _ in range(n)]
+        self.ag_out = [torch.empty(self.rc * n, dtype=torch.float32, device=dev) for _ in range(n)]
+        self.ll_w = [torch.zeros(rra.rra_ll_wire_bytes(self.llb), dtype=torch.uint8, device=dev)
+                     for _ in range(LL_SRC)]
+        self.l8_w = [torch.zeros(rra.rra_ll128_wire_bytes(self.llb), dtype=torch.uint8, device=dev)
+                     for _ in range(LL_SRC)]
+        self.ll_out = torch.empty(self.llb // 4, dtype=torch.int32, device=dev)
+        self.l8_out = torch.empty(self.llb // 4, dtype=torch.int32, device=dev)
+        S = self.count * 4
+        LW, L8 = rra.rra_ll_wire_bytes(self.llb), rra.rra_ll128_wire_bytes(self.llb)
+        B = self.llb
+        # (name, floor bytes, launches, bus bytes for busbw or None)
+        self.ops = [
+            ("ar_ring", floor_bytes("ar_", n, S), 1, S),
+            ("ar_oneshot", floor_bytes("ar_", n, S), 1, S),
+            ("ar_twoshot", floor_bytes("ar_", n, S), 1, S),
+            ("rs_ring", floor_bytes("rs_", n, S), 1, S),
+            ("rs_direct", floor_bytes("rs_", n, S), 1, S),
+            ("ag_ring", floor_bytes("ag_", n, S), 1, S),
+            ("ag_direct", floor_bytes("ag_", n, S), 1, S),
+            ("ll_pack", LL_SRC * (B + LW), LL_SRC, None),
+            ("ll_unpack", LL_SRC * LW + B, 1, None),
+            ("ll128_pack", LL_SRC * (B + L8), LL_SRC, None),
+            ("ll128_unpack", LL_SRC * L8 + B, 1, None),
+        ]
+        self.flag = 0
+
+    def run_op(self, name, stream):
+        rra, n = self.rra, N_RANKS
+        F, SUM = rra.RRA_FLOAT32, rra.RRA_SUM
+        if name == "ar_ring":
+            rra.rra_allreduce(self.x, self.ar_out, self.count, F, SUM, rra.RRA_ALGO_RING, stream)
+        elif name == "ar_oneshot":
+            rra.rra_allreduce(self.x, self.ar_out, self.count, F, SUM, rra.RRA_ALGO_ONE_SHOT, stream)
+        elif name == "ar_twoshot":
+            rra.rra_allreduce(self.x, self.ar_out, self.count, F, SUM, rra.RRA_ALGO_TWO_SHOT, stream)
+        elif name == "rs_ring":
+            rra.rra_reduce_scatter(self.x, self.rs_out, self.rc, F, SUM, rra.RRA_ALGO_RING, stream)
+        elif name == "rs_direct":
+            rra.rra_reduce_scatter(self.x, self.rs_out, self.rc, F, SUM, rra.RRA_ALGO_DIRECT, stream)
+        elif name == "ag_ring":
+            rra.rra_all_gather(self.sh, self.ag_out, self.rc, F, rra.RRA_ALGO_RING, stream)
+        elif name == "ag_direct":
+            rra.rra_all_gather(self.sh, self.ag_out, self.rc, F, rra.RRA_ALGO_DIRECT, stream)
+        elif name == "ll_pack":
+            for p, w in zip(self.pl, self.ll_w):
+                rra.rra_ll_pack(p, w, self.flag, stream=stream)
+        elif name == "ll_unpack":
+            rra.rra_ll_unpack(self.ll_w, self.ll_out, self.flag, stream=stream)
+        elif name == "ll128_pack":
+            for p, w in zip(self.pl, self.l8_w):
+                rra.rra_ll128_pack(p, w, self.flag, stream=stream)
+        elif name == "ll128_unpack":
+            rra.rra_ll128_unpack(self.l8_w, self.l8_out, self.flag, stream=stream)
+        else:
+            raise ValueError(name)
+
+    def launches(self):
+        return sum(k for _, _, k, _ in self.ops)
+
+    def floor(self):
+        return sum(b for _, b, _, _ in self.ops)
+
+
+def check_parity_sample(step, oracle):
+    """A few sampled elements of every output against sums the oracle's
+    arithmetic gives for them (the full comparison lives in the tests)."""
+    rng = np.random.default_rng(1)
+    idx = rng.integers(0, step.count, size=64)
+    xs = step.host["bucket"]
+    sub = [np.ascontiguousarray(x[idx]) for x in xs]
+    want, _, _ = oracle.allreduce("oneshot", sub, "float32")
+    got = step.ar_out[3].cpu().numpy()[idx]
+    return bool(np.array_equal(got, want[0]))
+
+
+def run_ours(args):
+    import torch
+
+    import collective_all_reduce_rank_gb300 as rra
+    from collective_all_reduce_rank_gb300 import inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    rra.rra_init(local)
+    step = Step(torch, rra, inputs, seed=rank)
+    stream = torch.cuda.Stream()
+    names = [o[0] for o in step.ops]
+
+    def one_step(ev=None):
+        step.flag += 1
+        for i, name in enumerate(names):
+            if ev is not None:
+                ev[i][0].record(stream)
+            step.run_op(name, stream)
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step()
+    torch.cuda.synchronize()
+    st, info = rra.rra_query_status(stream)
+    if st != 0:
+        raise RuntimeError("device status after warm-up: %d %s" % (st, info))
+
+    # timed region: K steps, per-op events on the launching stream
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in names] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for k in range(args.steps):
+                one_step(evs[k])
+            t1.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = t0.elapsed_time(t1)
+    st, info = rra.rra_query_status(stream)
+    if st != 0:
+        raise RuntimeError("device status after the timed steps: %d %s" % (st, info))
+    per_op = {n_: statistics.mean(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps))
+              for i, n_ in enumerate(names)}
+
+    # end to end through the public API: pinned host inputs -> device,
+    # the step, results -> pinned host, every step
+    h_x = [torch.from_numpy(x).pin_memory() for x in step.host["bucket"]]
+    h_sh = [torch.from_numpy(x).pin_memory() for x in step.host["shards"]]
+    h_pl = [torch.from_numpy(p).pin_memory() for p in step.host["payloads"]]
+    h_res = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in
+             (("ar", step.ar_out[0]), ("rs", step.rs_out[0]), ("ag", step.ag_out[0]),
+              ("ll", step.ll_out), ("l8", step.l8_out))}
+    h2d = sum(t.numel() * t.element_size() for t in h_x + h_sh + h_pl)
+    d2h = sum(t.numel() * t.element_size() for t in h_res.values())
+
+    def e2e_step():
+        for h, d in zip(h_x + h_sh + h_pl, step.x + step.sh + step.pl):
+            d.copy_(h, non_blocking=True)
+        one_step()
+        for k, d in (("ar", step.ar_out[0]), ("rs", step.rs_out[0]), ("ag", step.ag_out[0]),
+                     ("ll", step.ll_out), ("l8", step.l8_out)):
+            h_res[k].copy_(d, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    st, info = rra.rra_query_status(stream)
+    if st != 0:
+        raise RuntimeError("device status after the end-to-end steps: %d %s" % (st, info))
+
+    import oracle
+
+    parity = check_parity_sample(step, oracle)
+
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, "cuda")
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    floor = step.floor()
+    value = job_throughput(floor, world, args.steps, ms)
+    e2e_value = job_throughput(floor, world, e2e_steps, e2e_ms)
+    peak, peak_kind = peaks()
+    ops = {}
+    for name, fb, _, bus in step.ops:
+        t = per_op[name]
+        d = {"ms": round(t, 4), "GBps": round(fb / (t / 1e3) / 1e9, 1),
+             "pct_hbm_8TBps": round(100 * fb / (t / 1e3) / 1e9 / HBM_NOMINAL, 1),
+             "frac_of_measured": round(fb / (t / 1e3) / 1e9 / peak, 3)}
+        if bus is not None:
+            alg = bus / (t / 1e3) / 1e9
+            d["algbw"] = round(alg, 1)
+            d["busbw"] = round(alg * bus_factor(name, N_RANKS), 1)
+        ops[name] = d
+    # dominant kernel: the largest share of the step's device time among
+    # single-launch operations
+    dom = max((o for o in step.ops if o[2] == 1), key=lambda o: per_op[o[0]])
+    dom_name, dom_bytes = dom[0], dom[1]
+    achieved = dom_bytes / (per_op[dom_name] / 1e3) / 1e9
+    traffic = load_traffic(dom_name)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32,i32",
+        "data": "synthetic (seeded numpy PCG64; normal(0,1e-2) fp32 bucket, int32 in [-2^20,2^20])",
+        "config": {"workload": WORKLOAD, "n_virtual_ranks": N_RANKS, "bucket_elems_per_rank": step.count,
+                   "ll_payload_bytes": step.llb, "ll_sources": LL_SRC,
+                   "l2": "inputs larger than L2 (800 MB per AR op, 1 GiB LL payload); no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "traffic": traffic},
+        "ops": ops,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": step.launches() * args.steps,
+        "clocks": clk.summary(),
+        "parity_sample_ok": parity,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_scale)
+    if args.small:
+        line["tp_latency_us"] = tp_latency(torch, rra, inputs, stream)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of `values` over all ranks (the slowest replica
+    sets the time); identity without a process group."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(bytes_per_replica_step, world, steps, ms):
+    """Whole-job GB/s: every replica moves the same bytes per step; the time
+    is the slowest replica's."""
+    return world * bytes_per_replica_step * steps / (ms / 1e3) / 1e9
+
+
+def load_traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
+    None when the kernel's source has changed since it was captured."""
+    import hashlib
+
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))[kernel]
+    except Exception:
+        return None
+    src = os.path.join(ROOT, "collective_all_reduce_rank_gb300", "csrc", d["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return d["bytes_per_launch"] if h == d["source_sha"] else None
+
+
+# --------------------------------------------------------------------------
+# the oracle as the CPU baseline / reference arm
+# --------------------------------------------------------------------------
+def oracle_step(oracle, host, flag):
+    xs, sh, ps = host["bucket"], host["shards"], host["payloads"]
+    B = ps[0].size * 4
+    oracle.allreduce("ring", xs, "float32")
+    oracle.allreduce("oneshot", xs, "float32")
+    oracle.allreduce("twoshot", xs, "float32")
+    oracle.reduce_scatter("ring", xs, "float32")
+    oracle.reduce_scatter("direct", xs, "float32")
+    oracle.all_gather("ring", sh, "float32")
+    oracle.all_gather("direct", sh, "float32")
+    w = [oracle.ll_pack(p, flag) for p in ps]
+    oracle.ll_unpack(w, B, "int32", flag)
+    w = [oracle.ll128_pack(p, flag) for p in ps]
+    oracle.ll128_unpack(w, B, "int32", flag)
+
+
+def sample_host(scale, seed=0):
+    from collective_all_reduce_rank_gb300 import inputs
+
+    count = BUCKET // scale
+    xs = inputs.cfg_gradient_bucket(count, seed=seed)
+    return {"bucket": xs, "shards": [x[: count // N_RANKS].copy() for x in xs],
+            "payloads": inputs.cfg_ll_payloads(LL_BYTES // scale, LL_SRC, seed=seed)}
+
+
+def sample_floor(scale):
+    n = N_RANKS
+    S = (BUCKET // scale) * 4
+    B = LL_BYTES // scale
+    LW, L8 = 8 * ((B + 3) // 4), 128 * ((B + 119) // 120)
+    return (3 * floor_bytes("ar_", n, S) + 2 * floor_bytes("rs_", n, S) + 2 * floor_bytes("ag_", n, S)
+            + LL_SRC * (B + LW) + LL_SRC * LW + B + LL_SRC * (B + L8) + LL_SRC * L8 + B)
+
+
+def cpu_baseline(scale):
+    import oracle
+
+    host = sample_host(scale)
+    t = time.perf_counter()
+    oracle_step(oracle, host, 1)
+    dt = time.perf_counter() - t
+    return {"value": round(sample_floor(scale) / dt / 1e9, 3), "unit": UNIT, "cores": 1,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "one step at 1/%d of the workload (bucket %d elems/rank, LL payload %d B), "
+                      "single-threaded C oracle" % (scale, BUCKET // scale, LL_BYTES // scale)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    host = sample_host(args.cpu_scale)
+    for k in range(args.warmup):
+        oracle_step(oracle, host, k + 1)
+    t = time.perf_counter()
+    for k in range(args.steps):
+        oracle_step(oracle, host, k + 1)
+    dt = time.perf_counter() - t
+    value = sample_floor(args.cpu_scale) * args.steps / dt / 1e9
+    sample = ("each step = the whole step at 1/%d of the workload, single-threaded C oracle"
+              % args.cpu_scale)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32,i32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n_virtual_ranks": N_RANKS, "sample_scale": args.cpu_scale},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# tensor-parallel activations: small-message latency
+# --------------------------------------------------------------------------
+def tp_latency(torch, rra, inputs, stream, reps=200):
+    res = {}
+    for t in inputs.TP_TOKENS:
+        xs = inputs.cfg_tp_activations(t)
+        ins = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
+        outs = [torch.empty_like(x) for x in ins]
+        S = t * inputs.TP_HIDDEN * 2
+        row = {}
+        for name, algo in (("ring", rra.RRA_ALGO_RING), ("oneshot", rra.RRA_ALGO_ONE_SHOT),
+                           ("twoshot", rra.RRA_ALGO_TWO_SHOT), ("auto", rra.RRA_ALGO_AUTO)):
+            call = lambda: rra.rra_allreduce(ins, outs, t * inputs.TP_HIDDEN, rra.RRA_BFLOAT16,
+                                             rra.RRA_SUM, algo, stream)
+            with torch.cuda.stream(stream):
+                for _ in range(5):
+                    call()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(reps):
+                    call()
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            with torch.cuda.stream(stream):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / reps
+            alg = S / (us / 1e6) / 1e9
+            row[name] = {"us": round(us, 2), "algbw": round(alg, 1),
+                         "busbw": round(alg * 2 * (N_RANKS - 1) / N_RANKS, 1)}
+        res["tokens=%d" % t] = row
+    return res
+
+
+# --------------------------------------------------------------------------
+# message-size sweep (config 5) and the selector table
+# --------------------------------------------------------------------------
+def run_sweep(args):
+    import torch
+
+    import collective_all_reduce_rank_gb300 as rra
+    from collective_all_reduce_rank_gb300 import inputs
+
+    torch.cuda.set_device(0)
+    rra.rra_init(0)
+    stream = torch.cuda.Stream()
+    peak, _ = peaks()
+    algos = (("ring", rra.RRA_ALGO_RING), ("one_shot", rra.RRA_ALGO_ONE_SHOT),
+             ("two_shot", rra.RRA_ALGO_TWO_SHOT))
+    sizes = [s for s in inputs.SWEEP_SIZES if s <= args.sweep_max]
+    tune = []
+    out = open(args.sweep, "w")
+    for n in inputs.SWEEP_RANKS:
+        for dtype in ("int32", "bfloat16"):
+            code = rra.RRA_INT32 if dtype == "int32" else rra.RRA_BFLOAT16
+            tdt = torch.int32 if dtype == "int32" else torch.bfloat16
+            e = 4 if dtype == "int32" else 2
+            for S in sizes:
+                count = S // e
+                g = torch.Generator(device="cuda").manual_seed(S + n)
+                if dtype == "int32":
+                    ins = [torch.randint(-(1 << 20), (1 << 20) + 1, (count,), dtype=tdt, device="cuda",
+                                         generator=g) for _ in range(n)]
+                else:
+                    ins = [torch.randn(count, device="cuda", generator=g).to(tdt) for _ in range(n)]
+                outs = [torch.empty_like(x) for x in ins]
+                best = None
+                for name, algo in algos:
+                    call = lambda: rra.rra_allreduce(ins, outs, count, code, rra.RRA_SUM, algo, stream)
+                    us = time_call(torch, call, stream, S * n)
+                    fb = 2 * n * S
+                    alg = S / (us / 1e6) / 1e9
+                    row = {"n": n, "dtype": dtype, "bytes_per_rank": S, "algo": name, "us": round(us, 3),
+                           "algbw": round(alg, 2), "busbw": round(alg * 2 * (n - 1) / n, 2),
+                           "floor_bytes": fb, "GBps": round(fb / (us / 1e6) / 1e9, 1),
+                           "pct_hbm_8TBps": round(100 * fb / (us / 1e6) / 1e9 / HBM_NOMINAL, 1),
+                           "frac_of_measured": round(fb / (us / 1e6) / 1e9 / peak, 3),
+                           "l2_resident": 2 * n * S < 4 * (126 << 20)}
+                    out.write(json.dumps(row) + "\n")
+                    out.flush()
+                    if best is None or us < best[1]:
+                        best = (name, us)
+                tune.append((n, dtype, (S - 1).bit_length(), best[0]))
+                del ins, outs
+                torch.cuda.empty_cache()
+    out.close()
+    with open(args.sweep + ".tune.txt", "w") as f:
+        f.write("# nranks dtype log2_bytes algo  (fastest measured schedule per size)\n")
+        for n, dtype, lb, name in tune:
+            f.write("%d %s %d %s\n" % (n, dtype, lb, name))
+
+
+def time_call(torch, call, stream, total_bytes):
+    """Median microseconds per call: a CUDA graph of many calls for small
+    messages, single launches with events for large ones."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    torch.cuda.synchronize()
+    if total_bytes < (64 << 20):
+        reps = 100
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                call()
+        samples = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            with torch.cuda.stream(stream):
+                g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            samples.append(a.elapsed_time(b) * 1e3 / reps)
+        return statistics.median(samples)
+    samples = []
+    for _ in range(10 if total_bytes < (2 << 30) else 5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        samples.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(samples)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-scale", type=int, default=4, help="oracle sample = 1/scale of the workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true", help="add the TP-activation latency table")
+    ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")
+    ap.add_argument("--sweep-max", type=int, default=1 << 30)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,745 @@
+// rra_host.cpp -- the C ABI of include/rra.h: argument validation, the
+// chunk plan, algorithm selection, launch planning, device status, the
+// flight recorder and the tuning table.  Every computation of the
+// collectives runs in the kernels (kernels_*.cu); this file only decides
+// what to launch.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "rra.h"
+#include "rra_internal.h"
+
+using namespace rra;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kDefaultWorkspace = 64ull << 20;
+constexpr uint64_t kDefaultTimeoutNs = 500ull * 1000 * 1000;
+
+struct DevState {
+  bool ready = false;
+  int sms = 0;
+  char* base = nullptr;
+  size_t bytes = 0;
+  Workspace ws{};
+};
+
+DevState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+std::atomic<uint64_t> g_timeout_ns{0};
+std::atomic<int> g_skip_rank{-1};
+
+// ---------------------------------------------------------------------------
+// environment
+// ---------------------------------------------------------------------------
+long env_long(const char* name, long dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  char* end = nullptr;
+  const long x = std::strtol(v, &end, 10);
+  return (end && *end == 0) ? x : dflt;
+}
+
+bool debug_on() {
+  static const bool on = env_long("RRA_DEBUG", 0) != 0;
+  return on;
+}
+
+uint64_t timeout_ns() {
+  const uint64_t t = g_timeout_ns.load();
+  if (t) return t;
+  static const uint64_t env = (uint64_t)env_long("RRA_TIMEOUT_NS", 0);
+  return env ? env : kDefaultTimeoutNs;
+}
+
+size_t elem_size(rra_dtype_t dt) { return dt == RRA_BFLOAT16 ? 2 : 4; }
+
+const char* dtype_name(int dt) {
+  return dt == RRA_INT32 ? "int32" : dt == RRA_FLOAT32 ? "float32" : dt == RRA_BFLOAT16 ? "bfloat16" : "?";
+}
+
+const char* algo_name(int a) {
+  switch (a) {
+    case RRA_ALGO_AUTO: return "auto";
+    case RRA_ALGO_RING: return "ring";
+    case RRA_ALGO_ONE_SHOT: return "one_shot";
+    case RRA_ALGO_TWO_SHOT: return "two_shot";
+    case RRA_ALGO_DIRECT: return "direct";
+    default: return "?";
+  }
+}
+
+int parse_algo(const char* s) {
+  if (!s) return -1;
+  if (!std::strcmp(s, "ring")) return RRA_ALGO_RING;
+  if (!std::strcmp(s, "one_shot") || !std::strcmp(s, "oneshot")) return RRA_ALGO_ONE_SHOT;
+  if (!std::strcmp(s, "two_shot") || !std::strcmp(s, "twoshot")) return RRA_ALGO_TWO_SHOT;
+  if (!std::strcmp(s, "direct")) return RRA_ALGO_DIRECT;
+  return -1;
+}
+
+// ---------------------------------------------------------------------------
+// flight recorder: the last kRecent calls
+// ---------------------------------------------------------------------------
+constexpr int kRecent = 64;
+struct CallRec {
+  uint64_t seq;
+  const char* call;
+  int algo, n, dt, grid;
+  size_t count;
+  int status;
+};
+CallRec g_rec[kRecent];
+uint64_t g_seq = 0;
+std::mutex g_rec_mu;
+
+rra_status_t record(const char* call, int algo, int n, size_t count, int dt, int grid,
+                    rra_status_t st) {
+  {
+    std::lock_guard<std::mutex> lk(g_rec_mu);
+    CallRec& c = g_rec[g_seq % kRecent];
+    c = CallRec{g_seq, call, algo, n, dt, grid, count, (int)st};
+    ++g_seq;
+  }
+  if (debug_on())
+    std::fprintf(stderr, "[rra] %s algo=%s n=%d count=%zu dtype=%s grid=%d -> %s\n", call,
+                 algo_name(algo), n, count, dtype_name(dt), grid, rra_status_string(st));
+  return st;
+}
+
+// ---------------------------------------------------------------------------
+// tuning table
+// ---------------------------------------------------------------------------
+struct TuneEntry {
+  int n, dt, log2b, algo;
+};
+std::vector<TuneEntry> g_tune;
+std::mutex g_tune_mu;
+
+int ceil_log2(size_t x) {
+  int l = 0;
+  while (((size_t)1 << l) < x && l < 63) ++l;
+  return l;
+}
+
+// ---------------------------------------------------------------------------
+// validation helpers
+// ---------------------------------------------------------------------------
+bool valid_dtype(int dt) { return dt == RRA_INT32 || dt == RRA_FLOAT32 || dt == RRA_BFLOAT16; }
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool overlap(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return an && bn && x < y + bn && y < x + an;
+}
+
+// Input ranges may overlap one another (they are only read).  Output ranges
+// must be pairwise disjoint, and an output may meet an input only as the
+// exact in-place location allowed for that rank (inplace_in[r]).
+rra_status_t check_alias(const void* const* in, size_t in_bytes, void* const* out, size_t out_bytes,
+                         int n, const char* const* inplace_in) {
+  for (int i = 0; i < n; ++i)
+    for (int j = i + 1; j < n; ++j)
+      if (overlap(out[i], out_bytes, out[j], out_bytes)) return RRA_ERR_ALIAS;
+  for (int j = 0; j < n; ++j)
+    for (int i = 0; i < n; ++i) {
+      if (!overlap(out[j], out_bytes, in[i], in_bytes)) continue;
+      if (i == j && inplace_in && in[i] == (const void*)inplace_in[i]) continue;
+      return RRA_ERR_ALIAS;
+    }
+  return RRA_SUCCESS;
+}
+
+DevState* current_state(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (dev_out) *dev_out = dev;
+  return &g_dev[dev];
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < kMaxDevices && g_dev[dev].ready) return g_dev[dev].sms;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
+}
+
+WaitCfg wait_cfg(DevState* s) {
+  WaitCfg w;
+  w.status = s->ws.status;
+  w.sync = s->ws.sync;
+  w.timeout_ns = timeout_ns();
+  w.skip_rank = g_skip_rank.load();
+  return w;
+}
+
+rra_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return RRA_SUCCESS;
+  if (debug_on()) std::fprintf(stderr, "[rra] CUDA error: %s\n", cudaGetErrorString(e));
+  return RRA_ERR_CUDA;
+}
+
+// Grid for a grid-stride streaming kernel: enough CTAs to give every
+// thread work, at most what the GPU holds at once.
+int stream_grid(size_t units, int threads, int per_sm) {
+  const size_t want = (units + threads - 1) / threads;
+  const size_t cap = (size_t)sm_count() * (size_t)per_sm;
+  return (int)std::max<size_t>(1, std::min(want, cap));
+}
+
+// ---------------------------------------------------------------------------
+// launch planning for the persistent kernels
+// ---------------------------------------------------------------------------
+
+rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, int n, size_t count,
+                         rra_dtype_t dt, bool vec, cudaStream_t st, int* grid_out) {
+  TwoShotArgs a{};
+  const size_t e = elem_size(dt), pu = 16 / e;
+  const size_t per = (count + n - 1) / n;
+  const size_t clen = (per + pu - 1) / pu * pu;
+  for (int c = 0; c < n; ++c) {
+    a.in[c] = in[c];
+    a.out[c] = out[c];
+    const size_t lo = std::min(count, (size_t)c * clen), hi = std::min(count, (size_t)(c + 1) * clen);
+    a.chunk_lo[c] = lo;
+    a.chunk_len[c] = hi - lo;
+  }
+  a.tile_units = kDirectThreads * kTwoShotUnitsPerThread;
+  int occ = 0;
+  cudaError_t err = twoshot_occupancy(n, dt, vec, &occ);
+  if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
+  const size_t units0 = (a.chunk_len[0] + pu - 1) / pu;
+  const size_t need = (units0 + a.tile_units - 1) / a.tile_units;
+  long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need)});
+  c = std::min(c, env_long("RRA_TWOSHOT_CHANNELS", c));
+  if (c < 1) return RRA_ERR_UNSUPPORTED;
+  a.channels = (int)c;
+  a.progress = s->ws.flags + 2 * kLinkFlags;
+  a.wait = wait_cfg(s);
+  *grid_out = n * (int)c;
+  return cuda_status(launch_twoshot(n, dt, vec, a, n * (int)c, st));
+}
+
+// mode: kRingAllReduce / kRingReduceScatter / kRingAllGather.  ibase, obase,
+// len: per chunk, in elements.
+rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int n, int mode,
+                      const size_t* ibase, const size_t* obase, const size_t* len, rra_dtype_t dt,
+                      bool vec, cudaStream_t st, int* grid_out) {
+  RingArgs a{};
+  const size_t e = elem_size(dt), pu = 16 / e;
+  size_t maxu = 0;
+  for (int c = 0; c < n; ++c) {
+    a.in[c] = in[c];
+    a.out[c] = out[c];
+    a.ibase[c] = ibase[c];
+    a.obase[c] = obase[c];
+    a.len[c] = len[c];
+    maxu = std::max(maxu, (len[c] + pu - 1) / pu);
+  }
+  a.n = n;
+  a.mode = mode;
+  a.slice_units = kRingThreads * kRingUnitsPerThread;
+  // K > G: with K == G every rank could fill its outgoing FIFO in the first
+  // step and then wait for a credit its successor can only give after
+  // sending too (sends minus receives of a rank never exceed G, so n full
+  // FIFOs of K > G slots cannot all be pending at once).
+  a.G = (int)std::max(1L, env_long("RRA_RING_G", 4));
+  a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", 2L * a.G));
+  const int aw = dt == RRA_BFLOAT16 ? 2 : 1;
+  a.slot_bytes = (size_t)a.slice_units * 16 * aw;
+  int occ = 0;
+  cudaError_t err = ring_occupancy(dt, vec, &occ);
+  if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
+  const size_t need = (maxu + (size_t)a.G * a.slice_units - 1) / ((size_t)a.G * a.slice_units);
+  const size_t fifo_cap = s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes);
+  long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
+                           (long)fifo_cap, env_long("RRA_RING_CHANNELS", 16)});
+  if (c < 1) return RRA_ERR_UNSUPPORTED;
+  a.channels = (int)c;
+  a.fifo = s->ws.fifo;
+  a.head = s->ws.flags;
+  a.tail = s->ws.flags + kLinkFlags;
+  a.wait = wait_cfg(s);
+  *grid_out = n * (int)c;
+  return cuda_status(launch_ring(dt, vec, a, n * (int)c, st));
+}
+
+bool all_aligned16(const void* const* p, int n) {
+  for (int i = 0; i < n; ++i)
+    if (!aligned(p[i], 16)) return false;
+  return true;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char* rra_status_string(rra_status_t s) {
+  switch (s) {
+    case RRA_SUCCESS: return "success";
+    case RRA_ERR_INVALID_ARG: return "invalid argument";
+    case RRA_ERR_UNSUPPORTED: return "unsupported";
+    case RRA_ERR_ALIAS: return "buffers overlap";
+    case RRA_ERR_NOT_INITIALIZED: return "rra_init was not called for this device";
+    case RRA_ERR_CUDA: return "CUDA error";
+    case RRA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+rra_status_t rra_init(int device, size_t workspace_bytes) {
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev || device >= kMaxDevices)
+    return RRA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (cudaSetDevice(device) != cudaSuccess) return RRA_ERR_CUDA;
+  DevState& s = g_dev[device];
+  if (s.ready) return RRA_SUCCESS;
+  size_t bytes = workspace_bytes ? workspace_bytes : kDefaultWorkspace;
+  bytes = std::max<size_t>(bytes, 1u << 20);
+  char* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) return RRA_ERR_CUDA;
+  if (cudaMemset(p, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(p);
+    return RRA_ERR_CUDA;
+  }
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  s.base = p;
+  s.bytes = bytes;
+  s.sms = sms;
+  s.ws.status = reinterpret_cast<DevStatus*>(p);
+  s.ws.sync = reinterpret_cast<SyncHdr*>(p + 64);
+  s.ws.flags = reinterpret_cast<uint64_t*>(p + kFlagOffset);
+  s.ws.fifo = p + kFifoOffset;
+  s.ws.fifo_bytes = bytes > kFifoOffset ? bytes - kFifoOffset : 0;
+  s.ready = true;
+  return RRA_SUCCESS;
+}
+
+rra_status_t rra_finalize(int device) {
+  if (device < 0 || device >= kMaxDevices) return RRA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevState& s = g_dev[device];
+  if (!s.ready) return RRA_SUCCESS;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  cudaSetDevice(device);
+  cudaFree(s.base);
+  cudaSetDevice(cur);
+  s = DevState{};
+  return RRA_SUCCESS;
+}
+
+void rra_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
+
+void rra_debug_skip_rank(int rank) { g_skip_rank.store(rank); }
+
+rra_algo_t rra_select_algo(int nranks, size_t bytes_per_rank, rra_dtype_t dtype) {
+  if (nranks <= 1) return RRA_ALGO_ONE_SHOT;
+  {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    const int lb = ceil_log2(std::max<size_t>(1, bytes_per_rank));
+    int best_l = -1, best_a = -1;
+    for (const TuneEntry& t : g_tune)
+      if (t.n == nranks && t.dt == (int)dtype && t.log2b <= lb && t.log2b > best_l) {
+        best_l = t.log2b;
+        best_a = t.algo;
+      }
+    if (best_a >= 0) return (rra_algo_t)best_a;
+  }
+  // Prior: the alpha-beta model of the "Algorithms" section with one-GPU
+  // constants.  Every virtual rank's traffic crosses the same HBM, so beta
+  // is the HBM bandwidth; alpha is one flag round trip through L2.  One-shot
+  // (2 alpha + (n-1) S / beta) against two-shot (4 alpha + 2 (n-1)/n S /
+  // beta): one-shot up to S* = 2 alpha beta / ((n-1)(1-2/n)).
+  const double alpha = 2.0e-6, beta = 6.5e12;
+  const double den = (nranks - 1) * (1.0 - 2.0 / nranks);
+  if (den <= 0) return RRA_ALGO_ONE_SHOT;
+  const double s_star = 2 * alpha * beta / den;
+  return (double)bytes_per_rank <= s_star ? RRA_ALGO_ONE_SHOT : RRA_ALGO_TWO_SHOT;
+}
+
+rra_status_t rra_load_tuning(const char* path) {
+  if (!path) {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    g_tune.clear();
+    return RRA_SUCCESS;
+  }
+  FILE* f = std::fopen(path, "r");
+  if (!f) return RRA_ERR_INVALID_ARG;
+  std::vector<TuneEntry> t;
+  char line[256];
+  bool bad = false;
+  while (std::fgets(line, sizeof line, f)) {
+    char* hash = std::strchr(line, '#');
+    if (hash) *hash = 0;
+    char dts[32], al[32];
+    int n = 0, lb = 0;
+    const int got = std::sscanf(line, "%d %31s %d %31s", &n, dts, &lb, al);
+    if (got <= 0) continue;
+    if (got != 4) { bad = true; break; }
+    int dt = !std::strcmp(dts, "int32") ? RRA_INT32 : !std::strcmp(dts, "float32") ? RRA_FLOAT32
+             : !std::strcmp(dts, "bfloat16") ? RRA_BFLOAT16 : -1;
+    const int a = parse_algo(al);
+    if (dt < 0 || a < 0 || a == RRA_ALGO_DIRECT || n < 1 || n > kMaxRanks || lb < 0 || lb > 63) {
+      bad = true;
+      break;
+    }
+    t.push_back(TuneEntry{n, dt, lb, a});
+  }
+  std::fclose(f);
+  if (bad) return RRA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune.swap(t);
+  return RRA_SUCCESS;
+}
+
+rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nranks, size_t count,
+                           rra_dtype_t dtype, rra_op_t op, rra_algo_t algo, rra_stream_t stream) {
+  const char* call = "allreduce";
+  if (!bufs || !outs || nranks < 1 || !valid_dtype(dtype) || op != RRA_SUM || (int)algo < 0 ||
+      (int)algo > RRA_ALGO_TWO_SHOT)
+    return record(call, algo, nranks, count, dtype, 0,
+                  nranks > kMaxRanks ? RRA_ERR_UNSUPPORTED : RRA_ERR_INVALID_ARG);
+  if (nranks > kMaxRanks) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_UNSUPPORTED);
+  const size_t e = elem_size(dtype);
+  if (count > (SIZE_MAX / 2) / e) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_INVALID_ARG);
+  for (int r = 0; r < nranks; ++r)
+    if (!bufs[r] || !outs[r] || !aligned(bufs[r], e) || !aligned(outs[r], e))
+      return record(call, algo, nranks, count, dtype, 0, RRA_ERR_INVALID_ARG);
+  const size_t S = count * e;
+  const rra_status_t al = check_alias(bufs, S, outs, S, nranks, reinterpret_cast<const char* const*>(outs));
+  if (al != RRA_SUCCESS) return record(call, algo, nranks, count, dtype, 0, al);
+  if (algo == RRA_ALGO_AUTO) {
+    const int env = parse_algo(std::getenv("RRA_ALGO"));
+    algo = (env == RRA_ALGO_RING || env == RRA_ALGO_ONE_SHOT || env == RRA_ALGO_TWO_SHOT)
+               ? (rra_algo_t)env
+               : rra_select_algo(nranks, S, dtype);
+  }
+  if (count == 0) return record(call, algo, nranks, count, dtype, 0, RRA_SUCCESS);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool vec = all_aligned16(bufs, nranks) && all_aligned16((const void* const*)outs, nranks);
+  bool inplace_all = true;
+  for (int r = 0; r < nranks; ++r) inplace_all = inplace_all && bufs[r] == outs[r];
+  if (nranks == 1) {
+    if (inplace_all) return record(call, algo, 1, count, dtype, 0, RRA_SUCCESS);
+    DirectArgs a{};
+    a.in[0] = bufs[0];
+    a.out[0] = outs[0];
+    a.count = count;
+    int grid = 0;
+    const cudaError_t err = launch_oneshot(1, dtype, vec, a, (count * e + 15) / 16, &grid, st);
+    return record(call, algo, 1, count, dtype, grid, cuda_status(err));
+  }
+  if (algo == RRA_ALGO_ONE_SHOT) {
+    DirectArgs a{};
+    for (int r = 0; r < nranks; ++r) {
+      a.in[r] = bufs[r];
+      a.out[r] = outs[r];
+    }
+    a.count = count;
+    a.per_rank_grid = (int)env_long("RRA_ONESHOT_PER_RANK", 0) != 0;
+    int grid = 0;
+    const cudaError_t err = launch_oneshot(nranks, dtype, vec, a, (count * e + 15) / 16, &grid, st);
+    return record(call, algo, nranks, count, dtype, grid, cuda_status(err));
+  }
+  int dev = 0;
+  DevState* s = current_state(&dev);
+  if (!s || !s->ready) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_NOT_INITIALIZED);
+  int grid = 0;
+  rra_status_t rs;
+  if (algo == RRA_ALGO_TWO_SHOT) {
+    rs = run_twoshot(s, bufs, outs, nranks, count, dtype, vec, st, &grid);
+  } else {
+    const size_t pu = 16 / e;
+    const size_t per = (count + nranks - 1) / nranks;
+    const size_t clen = (per + pu - 1) / pu * pu;
+    size_t lo[kMaxRanks], len[kMaxRanks];
+    for (int c = 0; c < nranks; ++c) {
+      lo[c] = std::min(count, (size_t)c * clen);
+      len[c] = std::min(count, (size_t)(c + 1) * clen) - lo[c];
+    }
+    rs = run_ring(s, bufs, outs, nranks, kRingAllReduce, lo, lo, len, dtype, vec, st, &grid);
+  }
+  return record(call, algo, nranks, count, dtype, grid, rs);
+}
+
+rra_status_t rra_reduce_scatter(const void* const* bufs, void* const* outs, int nranks,
+                                size_t recvcount, rra_dtype_t dtype, rra_op_t op, rra_algo_t algo,
+                                rra_stream_t stream) {
+  const char* call = "reduce_scatter";
+  if (!bufs || !outs || nranks < 1 || !valid_dtype(dtype) || op != RRA_SUM || (int)algo < 0 ||
+      (int)algo > RRA_ALGO_DIRECT || algo == RRA_ALGO_ONE_SHOT)
+    return record(call, algo, nranks, recvcount, dtype, 0,
+                  nranks > kMaxRanks ? RRA_ERR_UNSUPPORTED : RRA_ERR_INVALID_ARG);
+  if (nranks > kMaxRanks) return record(call, algo, nranks, recvcount, dtype, 0, RRA_ERR_UNSUPPORTED);
+  const size_t e = elem_size(dtype);
+  if (recvcount > (SIZE_MAX / 2) / e / kMaxRanks)
+    return record(call, algo, nranks, recvcount, dtype, 0, RRA_ERR_INVALID_ARG);
+  for (int r = 0; r < nranks; ++r)
+    if (!bufs[r] || !outs[r] || !aligned(bufs[r], e) || !aligned(outs[r], e))
+      return record(call, algo, nranks, recvcount, dtype, 0, RRA_ERR_INVALID_ARG);
+  const size_t rbytes = recvcount * e;
+  const char* inplace[kMaxRanks];
+  for (int r = 0; r < nranks; ++r) inplace[r] = static_cast<const char*>(bufs[r]) + (size_t)r * rbytes;
+  // an in-place output sits inside its own input: allowed only at slice r
+  for (int r = 0; r < nranks; ++r)
+    if (overlap(outs[r], rbytes, bufs[r], rbytes * nranks) && (const char*)outs[r] != inplace[r])
+      return record(call, algo, nranks, recvcount, dtype, 0, RRA_ERR_ALIAS);
+  {
+    const void* ins[kMaxRanks];
+    for (int r = 0; r < nranks; ++r) ins[r] = bufs[r];
+    // outputs pairwise disjoint, and no output inside another rank's input
+    for (int i = 0; i < nranks; ++i)
+      for (int j = 0; j < nranks; ++j) {
+        if (i != j && overlap(outs[i], rbytes, outs[j], rbytes))
+          return record(call, algo, nranks, recvcount, dtype, 0, RRA_ERR_ALIAS);
+        if (i != j && overlap(outs[j], rbytes, ins[i], rbytes * nranks))
+          return record(call, algo, nranks, recvcount, dtype, 0, RRA_ERR_ALIAS);
+      }
+  }
+  if (algo == RRA_ALGO_AUTO) algo = RRA_ALGO_DIRECT;
+  if (algo == RRA_ALGO_TWO_SHOT) algo = RRA_ALGO_DIRECT;
+  if (recvcount == 0) return record(call, algo, nranks, recvcount, dtype, 0, RRA_SUCCESS);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool vec = all_aligned16(bufs, nranks) && all_aligned16((const void* const*)outs, nranks) &&
+                   (rbytes % 16) == 0;
+  if (algo == RRA_ALGO_DIRECT || nranks == 1) {
+    DirectArgs a{};
+    for (int r = 0; r < nranks; ++r) {
+      a.in[r] = bufs[r];
+      a.out[r] = outs[r];
+    }
+    a.count = recvcount;
+    int grid = 0;
+    const cudaError_t err = launch_direct_rs(nranks, dtype, vec, a, (rbytes + 15) / 16, &grid, st);
+    return record(call, algo, nranks, recvcount, dtype, grid, cuda_status(err));
+  }
+  DevState* s = current_state(nullptr);
+  if (!s || !s->ready) return record(call, algo, nranks, recvcount, dtype, 0, RRA_ERR_NOT_INITIALIZED);
+  size_t ib[kMaxRanks], ob[kMaxRanks], len[kMaxRanks];
+  for (int c = 0; c < nranks; ++c) {
+    ib[c] = (size_t)c * recvcount;
+    ob[c] = 0;
+    len[c] = recvcount;
+  }
+  int grid = 0;
+  const rra_status_t rs =
+      run_ring(s, bufs, outs, nranks, kRingReduceScatter, ib, ob, len, dtype, vec, st, &grid);
+  return record(call, algo, nranks, recvcount, dtype, grid, rs);
+}
+
+rra_status_t rra_all_gather(const void* const* bufs, void* const* outs, int nranks, size_t sendcount,
+                            rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
+  const char* call = "all_gather";
+  if (!bufs || !outs || nranks < 1 || !valid_dtype(dtype) || (int)algo < 0 ||
+      (int)algo > RRA_ALGO_DIRECT || algo == RRA_ALGO_ONE_SHOT)
+    return record(call, algo, nranks, sendcount, dtype, 0,
+                  nranks > kMaxRanks ? RRA_ERR_UNSUPPORTED : RRA_ERR_INVALID_ARG);
+  if (nranks > kMaxRanks) return record(call, algo, nranks, sendcount, dtype, 0, RRA_ERR_UNSUPPORTED);
+  const size_t e = elem_size(dtype);
+  if (sendcount > (SIZE_MAX / 2) / e / kMaxRanks)
+    return record(call, algo, nranks, sendcount, dtype, 0, RRA_ERR_INVALID_ARG);
+  for (int r = 0; r < nranks; ++r)
+    if (!bufs[r] || !outs[r] || !aligned(bufs[r], e) || !aligned(outs[r], e))
+      return record(call, algo, nranks, sendcount, dtype, 0, RRA_ERR_INVALID_ARG);
+  const size_t sbytes = sendcount * e;
+  for (int i = 0; i < nranks; ++i)
+    for (int j = 0; j < nranks; ++j) {
+      if (i != j && overlap(outs[i], sbytes * nranks, outs[j], sbytes * nranks))
+        return record(call, algo, nranks, sendcount, dtype, 0, RRA_ERR_ALIAS);
+      if (!overlap(outs[j], sbytes * nranks, bufs[i], sbytes)) continue;
+      // in place: shard i sits at slot i of its own output
+      if (i == j && bufs[i] == static_cast<const char*>(outs[i]) + (size_t)i * sbytes) continue;
+      return record(call, algo, nranks, sendcount, dtype, 0, RRA_ERR_ALIAS);
+    }
+  if (algo == RRA_ALGO_AUTO || algo == RRA_ALGO_TWO_SHOT) algo = RRA_ALGO_DIRECT;
+  if (sendcount == 0) return record(call, algo, nranks, sendcount, dtype, 0, RRA_SUCCESS);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool vec = all_aligned16(bufs, nranks) && all_aligned16((const void* const*)outs, nranks) &&
+                   (sbytes % 16) == 0;
+  if (algo == RRA_ALGO_DIRECT || nranks == 1) {
+    DirectArgs a{};
+    for (int r = 0; r < nranks; ++r) {
+      a.in[r] = bufs[r];
+      a.out[r] = outs[r];
+    }
+    a.count = sendcount;
+    int grid = 0;
+    const cudaError_t err = launch_direct_ag(nranks, dtype, vec, a, (sbytes + 15) / 16, &grid, st);
+    return record(call, algo, nranks, sendcount, dtype, grid, cuda_status(err));
+  }
+  DevState* s = current_state(nullptr);
+  if (!s || !s->ready) return record(call, algo, nranks, sendcount, dtype, 0, RRA_ERR_NOT_INITIALIZED);
+  size_t ib[kMaxRanks], ob[kMaxRanks], len[kMaxRanks];
+  for (int c = 0; c < nranks; ++c) {
+    ib[c] = 0;
+    ob[c] = (size_t)c * sendcount;
+    len[c] = sendcount;
+  }
+  int grid = 0;
+  const rra_status_t rs =
+      run_ring(s, bufs, outs, nranks, kRingAllGather, ib, ob, len, dtype, vec, st, &grid);
+  return record(call, algo, nranks, sendcount, dtype, grid, rs);
+}
+
+size_t rra_ll_wire_bytes(size_t payload_bytes) { return 8 * ((payload_bytes + 3) / 4); }
+
+size_t rra_ll128_wire_bytes(size_t payload_bytes) { return 128 * ((payload_bytes + 119) / 120); }
+
+static rra_status_t pack_common(const char* call, bool is128, const void* payload,
+                                size_t payload_bytes, void* wire, uint64_t flag, rra_stream_t stream) {
+  if (!payload || !wire || flag == 0 || !aligned(wire, 16) || payload_bytes > (SIZE_MAX / 4))
+    return record(call, 0, 1, payload_bytes, -1, 0, RRA_ERR_INVALID_ARG);
+  const size_t wbytes = is128 ? rra_ll128_wire_bytes(payload_bytes) : rra_ll_wire_bytes(payload_bytes);
+  if (overlap(payload, payload_bytes, wire, wbytes))
+    return record(call, 0, 1, payload_bytes, -1, 0, RRA_ERR_ALIAS);
+  if (payload_bytes == 0) return record(call, 0, 1, 0, -1, 0, RRA_SUCCESS);
+  LLArgs a{};
+  a.payload = payload;
+  a.wire_out = wire;
+  a.payload_bytes = payload_bytes;
+  a.flag = flag;
+  a.vec = aligned(payload, 16);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int grid;
+  cudaError_t e;
+  if (is128) {
+    const size_t quads = (payload_bytes + 479) / 480;
+    grid = stream_grid(quads * 32, kLLThreads, 8);
+    e = launch_ll128_pack(a, grid, st);
+  } else {
+    grid = stream_grid((payload_bytes + 15) / 16, kLLThreads, 8);
+    e = launch_ll_pack(a, grid, st);
+  }
+  return record(call, 0, 1, payload_bytes, -1, grid, cuda_status(e));
+}
+
+static rra_status_t unpack_common(const char* call, bool is128, const void* const* wires, int nsrc,
+                                  void* out, size_t payload_bytes, rra_dtype_t dtype, rra_op_t op,
+                                  uint64_t expected, rra_stream_t stream) {
+  if (!wires || !out || nsrc < 1 || !valid_dtype(dtype) || op != RRA_SUM || expected == 0 ||
+      payload_bytes % elem_size(dtype) || !aligned(out, elem_size(dtype)) || payload_bytes > (SIZE_MAX / 4))
+    return record(call, 0, nsrc, payload_bytes, dtype, 0,
+                  nsrc > kMaxRanks ? RRA_ERR_UNSUPPORTED : RRA_ERR_INVALID_ARG);
+  if (nsrc > kMaxRanks) return record(call, 0, nsrc, payload_bytes, dtype, 0, RRA_ERR_UNSUPPORTED);
+  const size_t wbytes = is128 ? rra_ll128_wire_bytes(payload_bytes) : rra_ll_wire_bytes(payload_bytes);
+  for (int k = 0; k < nsrc; ++k) {
+    if (!wires[k] || !aligned(wires[k], 16)) return record(call, 0, nsrc, payload_bytes, dtype, 0, RRA_ERR_INVALID_ARG);
+    if (overlap(wires[k], wbytes, out, payload_bytes))
+      return record(call, 0, nsrc, payload_bytes, dtype, 0, RRA_ERR_ALIAS);
+  }
+  if (payload_bytes == 0) return record(call, 0, nsrc, 0, dtype, 0, RRA_SUCCESS);
+  DevState* s = current_state(nullptr);
+  if (!s || !s->ready) return record(call, 0, nsrc, payload_bytes, dtype, 0, RRA_ERR_NOT_INITIALIZED);
+  LLArgs a{};
+  for (int k = 0; k < nsrc; ++k) a.wire_in[k] = wires[k];
+  a.out = out;
+  a.payload_bytes = payload_bytes;
+  a.flag = expected;
+  a.nsrc = nsrc;
+  a.vec = aligned(out, 16);
+  a.wait = wait_cfg(s);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int grid;
+  cudaError_t e;
+  if (is128) {
+    const size_t quads = (payload_bytes + 479) / 480;
+    grid = stream_grid(quads * 32, kLLThreads, 8);
+    e = launch_ll128_unpack(dtype, a, grid, st);
+  } else {
+    grid = stream_grid((payload_bytes + 15) / 16, kLLThreads, 8);
+    e = launch_ll_unpack(dtype, a, grid, st);
+  }
+  return record(call, 0, nsrc, payload_bytes, dtype, grid, cuda_status(e));
+}
+
+rra_status_t rra_ll_pack(const void* payload, size_t payload_bytes, void* wire, uint32_t flag,
+                         rra_stream_t stream) {
+  return pack_common("ll_pack", false, payload, payload_bytes, wire, flag, stream);
+}
+
+rra_status_t rra_ll128_pack(const void* payload, size_t payload_bytes, void* wire, uint64_t flag,
+                            rra_stream_t stream) {
+  return pack_common("ll128_pack", true, payload, payload_bytes, wire, flag, stream);
+}
+
+rra_status_t rra_ll_unpack(const void* const* wires, int nsrc, void* out, size_t payload_bytes,
+                           rra_dtype_t dtype, rra_op_t op, uint32_t expected_flag,
+                           rra_stream_t stream) {
+  return unpack_common("ll_unpack", false, wires, nsrc, out, payload_bytes, dtype, op, expected_flag,
+                       stream);
+}
+
+rra_status_t rra_ll128_unpack(const void* const* wires, int nsrc, void* out, size_t payload_bytes,
+                              rra_dtype_t dtype, rra_op_t op, uint64_t expected_flag,
+                              rra_stream_t stream) {
+  return unpack_common("ll128_unpack", true, wires, nsrc, out, payload_bytes, dtype, op,
+                       expected_flag, stream);
+}
+
+rra_status_t rra_query_status(rra_stream_t stream, int32_t info[4]) {
+  if (info) info[0] = info[1] = info[2] = info[3] = 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return RRA_ERR_CUDA;
+  DevState* s = current_state(nullptr);
+  if (!s || !s->ready) return RRA_SUCCESS;
+  DevStatus h{};
+  if (cudaMemcpy(&h, s->ws.status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return RRA_ERR_CUDA;
+  if (h.code == 0) return RRA_SUCCESS;
+  if (info) {
+    // prefer the wait on a peer that never posted: it names the rank that
+    // did not join, not one stuck behind it
+    const unsigned long long d = h.root_detail ? h.root_detail : h.detail;
+    const int peer = (int)((d >> 16) & 0xFFFF);
+    info[0] = h.code;
+    info[1] = (int)(d & 0xFFFF);
+    info[2] = peer == 0xFFFF ? -1 : peer;
+    info[3] = (int)((d >> 32) & 0x7FFFFFFF);
+  }
+  // clear the record; the abort tag belongs to a finished call and can stay
+  DevStatus z{};
+  z.abort_tag = h.abort_tag;
+  if (cudaMemcpy(s->ws.status, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return RRA_ERR_CUDA;
+  return (rra_status_t)h.code;
+}
+
+int rra_dump_recent(char* buf, size_t len) {
+  std::lock_guard<std::mutex> lk(g_rec_mu);
+  std::string s;
+  const uint64_t first = g_seq > kRecent ? g_seq - kRecent : 0;
+  int count = 0;
+  for (uint64_t q = first; q < g_seq; ++q) {
+    const CallRec& c = g_rec[q % kRecent];
+    char line[256];
+    std::snprintf(line, sizeof line, "%llu %s algo=%s n=%d count=%zu dtype=%s grid=%d status=%s\n",
+                  (unsigned long long)c.seq, c.call, algo_name(c.algo), c.n, c.count,
+                  dtype_name(c.dt), c.grid, rra_status_string((rra_status_t)c.status));
+    s += line;
+    ++count;
+  }
+  if (buf && len) {
+    const size_t m = std::min(len - 1, s.size());
+    std::memcpy(buf, s.data(), m);
+    buf[m] = 0;
+  }
+  return count;
+}
+
+}  // extern "C"

@@ -1,0 +1,157 @@
+// rra_internal.h -- what the host runtime (rra_host.cpp) and the kernel
+// files share: workspace layout, kernel argument structs, launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "rra.h"
+
+namespace rra {
+
+constexpr int kMaxRanks = RRA_MAX_RANKS;
+constexpr int kMaxChannels = 64;  // CTAs per virtual rank in persistent kernels
+
+// ---------------------------------------------------------------------------
+// workspace (one per device, made by rra_init, zero-filled)
+//
+//   [0, 64)        DevStatus: first device error + abort tag
+//   [64, 128)      SyncHdr: call epoch + end-of-kernel arrival counter
+//   [256, ...)     step flags, one uint64 per (link or rank, channel, warp):
+//                  ring head, ring tail, two-shot progress
+//   [kFifoOffset, end) ring FIFO slots
+// ---------------------------------------------------------------------------
+// A wait that expires records where: bit 63 set, bits 32..62 index (step
+// or line), bits 16..31 the rank waited for (0xFFFF: none), bits 0..15 the
+// waiting rank or LL source.  `detail` keeps the first such record;
+// `root_detail` one whose awaited peer posted nothing at all in the call
+// (the rank that never joined, rather than one stuck behind it).
+struct DevStatus {
+  int32_t code;                    // 0 or the first rra_status_t recorded on the device
+  uint32_t abort_tag;              // == tag of the call that gave up (epoch + 1)
+  unsigned long long detail;       // first expired wait
+  unsigned long long root_detail;  // expired wait on a peer that never posted
+  uint32_t pad[10];
+};
+static_assert(sizeof(DevStatus) == 64, "status block is one 64-byte line");
+
+struct SyncHdr {
+  uint32_t epoch;   // bumped by the last CTA of every synchronizing kernel
+  uint32_t arrive;  // CTAs of the running kernel that have finished
+  uint32_t pad[14];
+};
+
+constexpr int kMaxWarps = 16;  // warps per CTA of the persistent kernels (512 threads)
+constexpr size_t kFlagOffset = 256;
+constexpr size_t kLinkFlags = (size_t)kMaxRanks * kMaxChannels * kMaxWarps;
+constexpr size_t kFlagWords = 3 * kLinkFlags;  // ring head | ring tail | two-shot progress
+constexpr size_t kFifoOffset = 256 * 1024;
+static_assert(kFlagOffset + kFlagWords * 8 <= kFifoOffset, "flags fit below the FIFO");
+
+struct Workspace {
+  DevStatus* status;
+  SyncHdr* sync;
+  uint64_t* flags;  // kFlagWords entries
+  char* fifo;
+  size_t fifo_bytes;
+};
+
+// Settings every waiting kernel gets by value.
+struct WaitCfg {
+  DevStatus* status;
+  SyncHdr* sync;
+  uint64_t timeout_ns;
+  int skip_rank;  // fault injection: this rank posts nothing (-1: off)
+};
+
+// ---------------------------------------------------------------------------
+// kernel arguments
+// ---------------------------------------------------------------------------
+
+// One-shot all-reduce, direct reduce-scatter, direct all-gather.
+struct DirectArgs {
+  const void* in[kMaxRanks];
+  void* out[kMaxRanks];
+  size_t count;       // elements per unit range (AR: count, RS: recvcount, AG: sendcount)
+  int per_rank_grid;  // one-shot: 1 -> gridDim.y = n, block row r writes only out[r]
+};
+
+// Two-shot all-reduce (fused, persistent, cooperative).
+struct TwoShotArgs {
+  const void* in[kMaxRanks];
+  void* out[kMaxRanks];
+  size_t chunk_lo[kMaxRanks];   // element offset of chunk c
+  size_t chunk_len[kMaxRanks];  // elements in chunk c
+  uint64_t* progress;           // [(rank * channels + ch) * warps + warp]
+  int channels;
+  int tile_units;  // 16-byte units per tile per iteration
+  WaitCfg wait;
+};
+
+// Ring (persistent, cooperative): all-reduce, reduce-scatter or all-gather.
+enum RingMode : int { kRingAllReduce = 0, kRingReduceScatter = 1, kRingAllGather = 2 };
+
+struct RingArgs {
+  const void* in[kMaxRanks];
+  void* out[kMaxRanks];
+  size_t ibase[kMaxRanks];  // element offset of chunk c inside a rank's input
+  size_t obase[kMaxRanks];  // element offset of chunk c inside a rank's output
+  size_t len[kMaxRanks];    // elements in chunk c
+  char* fifo;               // links * slots * slot_bytes
+  uint64_t* head;           // [link * warps + warp]: messages posted by the sender
+  uint64_t* tail;           // [link * warps + warp]: messages consumed by the receiver
+  size_t slot_bytes;
+  int n;
+  int channels;
+  int mode;
+  int slice_units;  // 16-byte units per message (= blockDim * units per thread)
+  int G;            // messages per step and iteration
+  int K;            // FIFO slots per link
+  WaitCfg wait;
+};
+
+struct LLArgs {
+  const void* wire_in[kMaxRanks];
+  void* out;
+  const void* payload;
+  void* wire_out;
+  size_t payload_bytes;
+  uint64_t flag;  // pack: flag to write; unpack: expected flag
+  int nsrc;
+  int vec;  // payload / out 16-byte aligned
+  WaitCfg wait;
+};
+
+// ---------------------------------------------------------------------------
+// launchers (kernels_*.cu); all return the launch's cudaError_t
+// ---------------------------------------------------------------------------
+constexpr int kDirectThreads = 512;
+constexpr int kRingThreads = 512;
+constexpr int kRingUnitsPerThread = 2;
+constexpr int kTwoShotUnitsPerThread = 2;
+constexpr int kLLThreads = 256;
+
+// Streaming kernels: `units` 16-byte units per grid row; *grid receives the
+// CTAs per row launched.
+cudaError_t launch_oneshot(int n, int dt, bool vec, const DirectArgs& a, size_t units, int* grid,
+                           cudaStream_t s);
+cudaError_t launch_direct_rs(int n, int dt, bool vec, const DirectArgs& a, size_t units, int* grid,
+                             cudaStream_t s);
+cudaError_t launch_direct_ag(int n, int dt, bool vec, const DirectArgs& a, size_t units, int* grid,
+                             cudaStream_t s);
+
+// Persistent kernels are launched cooperatively: every CTA is resident or
+// the launch fails.  *max_blocks_per_sm reports the occupancy limit.
+cudaError_t twoshot_occupancy(int n, int dt, bool vec, int* max_blocks_per_sm);
+cudaError_t launch_twoshot(int n, int dt, bool vec, const TwoShotArgs& a, int grid, cudaStream_t s);
+cudaError_t ring_occupancy(int dt, bool vec, int* max_blocks_per_sm);
+cudaError_t launch_ring(int dt, bool vec, const RingArgs& a, int grid, cudaStream_t s);
+
+cudaError_t launch_ll_pack(const LLArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_ll_unpack(int dt, const LLArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_ll128_pack(const LLArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_ll128_unpack(int dt, const LLArgs& a, int grid, cudaStream_t s);
+
+}  // namespace rra

@@ -1,0 +1,253 @@
+/*
+ * rra.h -- all-reduce, reduce-scatter and all-gather over N "virtual ranks"
+ * held as separate buffers in one GPU's memory, plus the LL and LL128 wire
+ * formats.  Plain C ABI: device and host pointers, sizes and enums; no C++
+ * or PyTorch types.  Library: librra.so (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [ILP] "NCCL collectives, ring all-reduce & launching TP/PP"
+ *         (inference-learning-path): "Direct answer", "Deep dive", "Code".
+ *   [AIH] "Collective communication: NCCL's algorithms and protocols, and
+ *         custom all-reduce in inference frameworks" (ai-infra-handbooks):
+ *         "Algorithms: the ways to run one all-reduce", "Protocols: how do
+ *         you know the data has arrived", "Reading nccl-tests",
+ *         "Common environment variables and debugging", "Exercises" 2 and 3.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - A virtual rank r owns one input buffer bufs[r] and one output buffer
+ *   outs[r], all device pointers on the current CUDA device.  bufs/outs are
+ *   HOST arrays of nranks device pointers; they are read during the call
+ *   only (copied into the kernel's parameters), never retained.
+ * - Buffers are dense, 1-D, element type `dtype`, little-endian.  Each
+ *   pointer must be aligned to the element size; 16-byte aligned buffers
+ *   (what cudaMalloc and PyTorch give) take the 128-bit vector path, other
+ *   alignments a slower element-wise path with identical results.
+ * - The caller owns every buffer.  The library owns only the workspace made
+ *   by rra_init() for the device.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream), never allocate, never synchronize, and may be captured
+ *   into a CUDA graph.  Argument errors are returned synchronously before
+ *   any launch.  Errors found on the device (a bounded wait that expired, a
+ *   wire flag that never matched) are recorded in the device status word
+ *   and read with rra_query_status(), like an asynchronous communicator
+ *   error.
+ * - Calls that use the workspace (ring, two-shot, LL/LL128 unpack) on one
+ *   device must not overlap on the GPU: issue them on one stream or order
+ *   them, as with the operations of one communicator.
+ * - count == 0 returns RRA_SUCCESS without a launch.
+ * - Summation (op RRA_SUM): int32 wraps modulo 2^32; float32 adds in IEEE
+ *   round-to-nearest in the order the schedule fixes; bfloat16 is widened
+ *   to float32, summed in float32 in that order and rounded to bfloat16
+ *   (nearest, ties to even) once, when the final value is stored.
+ */
+#ifndef RRA_H
+#define RRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/** Same object as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* rra_stream_t;
+
+/** Largest number of virtual ranks (and of LL/LL128 sources) per call. */
+#define RRA_MAX_RANKS 8
+
+typedef enum {
+  RRA_SUCCESS = 0,
+  RRA_ERR_INVALID_ARG = 1,     /* null pointer, bad count, bad enum, misaligned pointer, flag 0 */
+  RRA_ERR_UNSUPPORTED = 2,     /* valid but not supported here (e.g. nranks > RRA_MAX_RANKS) */
+  RRA_ERR_ALIAS = 3,           /* input and output ranges overlap other than in place */
+  RRA_ERR_NOT_INITIALIZED = 4, /* rra_init() was not called for the current device */
+  RRA_ERR_CUDA = 5,            /* a CUDA runtime call failed (launch, query) */
+  RRA_ERR_TIMEOUT = 6          /* a bounded device wait expired (see rra_query_status) */
+} rra_status_t;
+
+typedef enum { RRA_INT32 = 0, RRA_FLOAT32 = 1, RRA_BFLOAT16 = 2 } rra_dtype_t;
+
+typedef enum { RRA_SUM = 0 } rra_op_t;
+
+/** Schedules ([AIH] "Algorithms").  For reduce-scatter and all-gather,
+ *  RRA_ALGO_DIRECT names the direct halves of two-shot (RRA_ALGO_TWO_SHOT
+ *  is accepted as a synonym) and RRA_ALGO_RING the ring halves. */
+typedef enum {
+  RRA_ALGO_AUTO = 0,
+  RRA_ALGO_RING = 1,
+  RRA_ALGO_ONE_SHOT = 2,
+  RRA_ALGO_TWO_SHOT = 3,
+  RRA_ALGO_DIRECT = 4
+} rra_algo_t;
+
+/* ------------------------------------------------------------------------ */
+/* set-up                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/** Create the per-device state: the workspace (device status word, step
+ *  flags, ring FIFO slots) of `workspace_bytes` bytes (0 = 64 MiB, at least
+ *  1 MiB) on CUDA device `device`, which becomes current.  Fixed buffers
+ *  made once, ahead of the calls, keep every call allocation-free and
+ *  graph-capturable, as [AIH] "Exercises" 3 explains for custom
+ *  all-reduce.  Calling it again for an initialised device is a no-op that
+ *  returns RRA_SUCCESS.  Errors: RRA_ERR_INVALID_ARG (bad device),
+ *  RRA_ERR_CUDA (allocation failed). */
+rra_status_t rra_init(int device, size_t workspace_bytes);
+
+/** Free the state of `device`.  The caller must have synchronized every
+ *  stream that used it. */
+rra_status_t rra_finalize(int device);
+
+/* ------------------------------------------------------------------------ */
+/* collectives                                                              */
+/* ------------------------------------------------------------------------ */
+
+/** All-reduce ([ILP] "Direct answer": sum a tensor every rank holds; every
+ *  rank ends with the result).  outs[r][i] = SUM_k bufs[k][i] for
+ *  i < count, every r.
+ *  - bufs[r], outs[r]: count elements each.  In place (outs[r] == bufs[r]
+ *    for every r) is allowed; any other overlap is RRA_ERR_ALIAS.
+ *  - algo: RING -- n-1 reduce-scatter steps then n-1 all-gather steps over
+ *    the N chunks of the chunk plan ([ILP] "Deep dive", [AIH] "Algorithms");
+ *    chunk c is summed in the order x_{c+1}, ..., x_{c-1}, x_c.
+ *    ONE_SHOT -- every rank's result read directly from all n inputs,
+ *    summed in ascending rank order.  TWO_SHOT -- rank r reduces chunk r
+ *    (ascending order), then every rank reads the reduced chunks back.
+ *    AUTO -- rra_select_algo().
+ *  - Chunk plan: chunk length C = ceil(count/n) rounded up to whole
+ *    16-byte vectors, chunk c = [min(cC,count), min((c+1)C,count)).
+ *  - nranks in [1, RRA_MAX_RANKS]; nranks == 1 copies (or does nothing in
+ *    place).
+ *  Errors: RRA_ERR_INVALID_ARG, RRA_ERR_UNSUPPORTED, RRA_ERR_ALIAS,
+ *  RRA_ERR_NOT_INITIALIZED (RING/TWO_SHOT/AUTO without rra_init),
+ *  RRA_ERR_CUDA. */
+rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nranks, size_t count,
+                           rra_dtype_t dtype, rra_op_t op, rra_algo_t algo, rra_stream_t stream);
+
+/** Reduce-scatter ([ILP] "Direct answer": sum across ranks, each keeps only
+ *  its slice).  bufs[r] holds nranks*recvcount elements; outs[r]
+ *  (recvcount elements) receives slice r of the sum:
+ *  outs[r][i] = SUM_k bufs[k][r*recvcount + i].
+ *  - algo RING: chunk c is summed x_{c+1}, ..., x_{c-1}, x_c (the ring's
+ *    reduce-scatter half).  DIRECT/TWO_SHOT/AUTO: ascending rank order.
+ *  - In place: outs[r] == bufs[r] + r*recvcount elements for every r.
+ *  Errors as rra_allreduce; ONE_SHOT is RRA_ERR_INVALID_ARG. */
+rra_status_t rra_reduce_scatter(const void* const* bufs, void* const* outs, int nranks,
+                                size_t recvcount, rra_dtype_t dtype, rra_op_t op, rra_algo_t algo,
+                                rra_stream_t stream);
+
+/** All-gather ([ILP] "Direct answer": each rank holds a shard, every rank
+ *  ends with the concatenation).  bufs[r] holds sendcount elements; outs[r]
+ *  holds nranks*sendcount: outs[r][q*sendcount + i] = bufs[q][i].
+ *  - algo RING: the ring's all-gather half (n-1 forwarding steps).
+ *    DIRECT/TWO_SHOT/AUTO: every rank reads every shard directly.
+ *  - In place: bufs[r] == outs[r] + r*sendcount elements for every r.
+ *  The data are copied bit for bit, whatever dtype says.
+ *  Errors as rra_allreduce; ONE_SHOT is RRA_ERR_INVALID_ARG. */
+rra_status_t rra_all_gather(const void* const* bufs, void* const* outs, int nranks,
+                            size_t sendcount, rra_dtype_t dtype, rra_algo_t algo,
+                            rra_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* LL and LL128 wire formats ([AIH] "Protocols")                            */
+/* ------------------------------------------------------------------------ */
+
+/** Bytes of LL wire for a payload: 8 * ceil(payload_bytes / 4).  LL: every
+ *  8-byte line holds 4 bytes of data and a 4-byte flag (50% efficiency). */
+size_t rra_ll_wire_bytes(size_t payload_bytes);
+
+/** Bytes of LL128 wire: 128 * ceil(payload_bytes / 120).  LL128: every
+ *  128-byte line holds 120 bytes of data and an 8-byte flag (93.75%). */
+size_t rra_ll128_wire_bytes(size_t payload_bytes);
+
+/** LL pack: line i of `wire` (device, 16-byte aligned,
+ *  rra_ll_wire_bytes(payload_bytes) bytes) gets payload bytes [4i, 4i+4) in
+ *  its bytes 0..3 (zero past the payload's end) and `flag` (little-endian)
+ *  in bytes 4..7.  Lines are written with single 16-byte stores, so a
+ *  line's data and flag become visible together.  flag must be nonzero (0
+ *  marks an empty line); callers use a step counter 1, 2, ...  `payload`
+ *  is a device pointer (any alignment).  Errors: RRA_ERR_INVALID_ARG. */
+rra_status_t rra_ll_pack(const void* payload, size_t payload_bytes, void* wire, uint32_t flag,
+                         rra_stream_t stream);
+
+/** LL unpack-and-reduce: for every line, poll each of the nsrc wires until
+ *  its flag equals expected_flag (a bounded wait, rra_set_timeout_ns), then
+ *  write the element-wise SUM of the nsrc data words, sources in ascending
+ *  order, to out (payload_bytes bytes, a whole number of dtype elements).
+ *  nsrc == 1 is a plain unpack.  wires: host array of nsrc device pointers
+ *  (16-byte aligned).  A line whose flag never matches ends the wait with
+ *  RRA_ERR_TIMEOUT in the status word: info = {code, source, -1, line}.
+ *  Needs rra_init().  Errors: RRA_ERR_INVALID_ARG, RRA_ERR_UNSUPPORTED,
+ *  RRA_ERR_NOT_INITIALIZED. */
+rra_status_t rra_ll_unpack(const void* const* wires, int nsrc, void* out, size_t payload_bytes,
+                           rra_dtype_t dtype, rra_op_t op, uint32_t expected_flag,
+                           rra_stream_t stream);
+
+/** LL128 pack: line j (128 bytes) of `wire` gets payload bytes
+ *  [120j, 120j+120) in bytes 0..119 (zero past the end) and `flag` as a
+ *  little-endian uint64 in bytes 120..127.  A warp writes four lines with
+ *  32 16-byte stores.  Other rules as rra_ll_pack. */
+rra_status_t rra_ll128_pack(const void* payload, size_t payload_bytes, void* wire, uint64_t flag,
+                            rra_stream_t stream);
+
+/** LL128 unpack-and-reduce: a warp reads four lines of each source (one
+ *  16-byte load per lane), checks the four flags across the warp, and on a
+ *  match sums the 120 data bytes of every line over the sources (ascending
+ *  order).  Other rules as rra_ll_unpack. */
+rra_status_t rra_ll128_unpack(const void* const* wires, int nsrc, void* out, size_t payload_bytes,
+                              rra_dtype_t dtype, rra_op_t op, uint64_t expected_flag,
+                              rra_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* status, selection, configuration                                         */
+/* ------------------------------------------------------------------------ */
+
+/** Synchronize `stream`, then read and clear the current device's status
+ *  word.  Returns RRA_SUCCESS, the recorded device error (RRA_ERR_TIMEOUT)
+ *  or RRA_ERR_CUDA if the stream itself failed.  info (may be NULL)
+ *  receives {code, rank, peer, index}: the rank (or LL source) whose wait
+ *  expired, the rank it waited for (-1 if none) and the step (ring,
+ *  two-shot) or line (LL, LL128) index. */
+rra_status_t rra_query_status(rra_stream_t stream, int32_t info[4]);
+
+/** The schedule AUTO uses for an all-reduce of bytes_per_rank bytes per
+ *  rank: from the measured table (rra_load_tuning) when one is loaded,
+ *  else from the alpha-beta cost model of [AIH] "Algorithms" with this
+ *  GPU's constants (one-shot up to the model's crossover, [AIH]
+ *  "Exercises" 2, two-shot above it).  Never returns RRA_ALGO_AUTO. */
+rra_algo_t rra_select_algo(int nranks, size_t bytes_per_rank, rra_dtype_t dtype);
+
+/** Load a tuning table: text lines "nranks dtype log2_bytes algo" (dtype
+ *  int32|float32|bfloat16, algo ring|one_shot|two_shot); '#' starts a
+ *  comment.  The entry with the largest log2_bytes <= ceil(log2(bytes))
+ *  for (nranks, dtype) wins.  NULL clears the table.  Errors:
+ *  RRA_ERR_INVALID_ARG (unreadable or malformed file; the old table stays). */
+rra_status_t rra_load_tuning(const char* path);
+
+/** Upper bound, in nanoseconds of %globaltimer, on every device-side wait
+ *  (ring and two-shot step flags, LL/LL128 line flags).  Default 500 ms
+ *  or RRA_TIMEOUT_NS from the environment; 0 restores the default. */
+void rra_set_timeout_ns(uint64_t ns);
+
+/** Fault injection for tests: virtual rank `rank` posts no step flag in the
+ *  following ring and two-shot calls (-1 turns it off), so its peers' waits
+ *  expire with RRA_ERR_TIMEOUT naming it as `peer`.  The GPU stays usable. */
+void rra_debug_skip_rank(int rank);
+
+/** Static text for a status code. */
+const char* rra_status_string(rra_status_t status);
+
+/** Flight recorder ([AIH] "Common environment variables and debugging":
+ *  a record of each rank's recent collectives): writes the last calls
+ *  (sequence number, call, algo, nranks, count, dtype, grid, result), one
+ *  per line, oldest first, into buf (NUL-terminated, truncated to len).
+ *  Returns the number of calls written. */
+int rra_dump_recent(char* buf, size_t len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RRA_H */

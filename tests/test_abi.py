@@ -1,0 +1,130 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and rejects bad arguments synchronously, before any launch."""
+import ctypes
+import math
+import os
+
+import pytest
+
+import collective_all_reduce_rank_gb300 as rra
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return rra.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = rra.header_symbols()
+    assert len(names) >= 18
+    for name in names:
+        assert hasattr(lib, name), name
+    # nothing from the oracle leaks into the product library
+    out = os.popen("nm -D --defined-only %s" % rra.library_path()).read()
+    assert "orc_" not in out
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert rra.rra_status_string(code)
+    assert "timed out" in rra.rra_status_string(rra.RRA_ERR_TIMEOUT)
+
+
+@pytest.mark.parametrize("B", [0, 1, 3, 4, 5, 119, 120, 121, 1 << 20])
+def test_wire_sizes(lib, B):
+    assert rra.rra_ll_wire_bytes(B) == 8 * math.ceil(B / 4)
+    assert rra.rra_ll128_wire_bytes(B) == 128 * math.ceil(B / 120)
+
+
+def _ar(bufs, outs, n, count, dtype=rra.RRA_FLOAT32, op=rra.RRA_SUM, algo=rra.RRA_ALGO_ONE_SHOT):
+    return rra.rra_allreduce(bufs, outs, count, dtype, op, algo, check=False, nranks=n)
+
+
+def test_argument_errors_return_before_launch(lib):
+    A = 1 << 40  # fake, never dereferenced: every case fails validation first
+    ins = [A + i * (1 << 30) for i in range(8)]
+    outs = [A + (16 << 30) + i * (1 << 30) for i in range(8)]
+    assert _ar(ins, outs, 0, 10) == rra.RRA_ERR_INVALID_ARG
+    assert _ar(ins + [A], outs + [A], 9, 10) == rra.RRA_ERR_UNSUPPORTED
+    assert _ar(ins, outs, 2, 10, dtype=7) == rra.RRA_ERR_INVALID_ARG
+    assert _ar(ins, outs, 2, 10, op=3) == rra.RRA_ERR_INVALID_ARG
+    assert _ar(ins, outs, 2, 10, algo=9) == rra.RRA_ERR_INVALID_ARG
+    assert _ar(ins, outs, 2, 10, algo=rra.RRA_ALGO_DIRECT) == rra.RRA_ERR_INVALID_ARG
+    assert _ar([0, ins[1]], outs, 2, 10) == rra.RRA_ERR_INVALID_ARG
+    assert _ar([ins[0] + 2, ins[1]], outs, 2, 10) == rra.RRA_ERR_INVALID_ARG  # not float-aligned
+    # bfloat16 needs only 2-byte alignment
+    assert _ar([ins[0] + 2, ins[1]], outs, 2, 0, dtype=rra.RRA_BFLOAT16) == rra.RRA_SUCCESS
+    # overlapping outputs, output inside another rank's input
+    assert _ar(ins, [outs[0], outs[0] + 8], 2, 10) == rra.RRA_ERR_ALIAS
+    assert _ar(ins, [ins[1], outs[1]], 2, 10) == rra.RRA_ERR_ALIAS
+    assert _ar(ins, [ins[0] + 4, outs[1]], 2, 10) == rra.RRA_ERR_ALIAS  # partial overlap
+    # in place is fine; count 0 launches nothing
+    assert _ar(ins, ins, 8, 0) == rra.RRA_SUCCESS
+    assert _ar(ins, outs, 8, 0, algo=rra.RRA_ALGO_RING) == rra.RRA_SUCCESS
+
+
+def test_rs_ag_argument_errors(lib):
+    A = 1 << 40
+    ins = [A + i * (1 << 30) for i in range(4)]
+    outs = [A + (16 << 30) + i * (1 << 30) for i in range(4)]
+    rs = lambda o, algo=rra.RRA_ALGO_DIRECT, c=10: rra.rra_reduce_scatter(
+        ins, o, c, rra.RRA_FLOAT32, rra.RRA_SUM, algo, check=False, nranks=4)
+    ag = lambda b, o, algo=rra.RRA_ALGO_DIRECT, c=10: rra.rra_all_gather(
+        b, o, c, rra.RRA_FLOAT32, algo, check=False, nranks=4)
+    assert rs(outs, rra.RRA_ALGO_ONE_SHOT) == rra.RRA_ERR_INVALID_ARG
+    # in place RS: out r at slice r of its own input
+    assert rs([ins[r] + r * 40 for r in range(4)], c=0) == rra.RRA_SUCCESS
+    assert rs([ins[r] + 40 for r in range(4)]) == rra.RRA_ERR_ALIAS
+    assert ag(ins, outs, rra.RRA_ALGO_ONE_SHOT) == rra.RRA_ERR_INVALID_ARG
+    # in place AG: shard r at slot r of its own output
+    assert ag([outs[r] + r * 40 for r in range(4)], outs, c=0) == rra.RRA_SUCCESS
+    assert ag([outs[r] for r in range(4)], outs) == rra.RRA_ERR_ALIAS
+
+
+def test_ll_argument_errors(lib):
+    A = 1 << 40
+    assert rra.rra_ll_pack(A, A + (1 << 30), 0, payload_bytes=16, check=False) == rra.RRA_ERR_INVALID_ARG
+    assert rra.rra_ll_pack(A, A + (1 << 30) + 8, 1, payload_bytes=16, check=False) == rra.RRA_ERR_INVALID_ARG
+    assert rra.rra_ll128_pack(A, A + 64, 1, payload_bytes=1024, check=False) == rra.RRA_ERR_ALIAS
+    wires = [A + i * (1 << 30) for i in range(9)]
+    out = A + (32 << 30)
+    u = lambda w, **k: rra.rra_ll_unpack(w, out, 1, dtype=rra.RRA_INT32, payload_bytes=k.get("B", 64),
+                                          check=False, nsrc=k.get("nsrc", len(w)))
+    assert u(wires[:9]) == rra.RRA_ERR_UNSUPPORTED
+    assert u(wires[:2], B=6) == rra.RRA_ERR_INVALID_ARG  # not whole int32 elements
+    assert rra.rra_ll128_unpack(wires[:2], out, 0, dtype=rra.RRA_INT32, payload_bytes=64,
+                                check=False) == rra.RRA_ERR_INVALID_ARG
+
+
+def test_flight_recorder_records_rejections(lib):
+    A = 1 << 40
+    rra.rra_allreduce([A, A + (1 << 30)], [A + (2 << 30), A + (3 << 30)], 0, rra.RRA_INT32,
+                      rra.RRA_SUM, rra.RRA_ALGO_RING, check=False)
+    rra.rra_allreduce([A, A + (1 << 30)], [A + (2 << 30), A + (2 << 30)], 5, rra.RRA_INT32,
+                      rra.RRA_SUM, rra.RRA_ALGO_RING, check=False)
+    text = rra.rra_dump_recent().strip().splitlines()
+    assert "algo=ring n=2 count=0 dtype=int32" in text[-2] and text[-2].endswith("status=success")
+    assert text[-1].endswith("status=buffers overlap")
+
+
+def test_selector_prior_and_tuning_table(lib, tmp_path):
+    rra.rra_load_tuning(None)
+    # prior: one-shot below the alpha-beta crossover, two-shot above; n=2 and
+    # n=1 always one-shot (the crossover's denominator vanishes)
+    assert rra.rra_select_algo(8, 4096, rra.RRA_BFLOAT16) == rra.RRA_ALGO_ONE_SHOT
+    assert rra.rra_select_algo(8, 1 << 30, rra.RRA_BFLOAT16) == rra.RRA_ALGO_TWO_SHOT
+    assert rra.rra_select_algo(2, 1 << 30, rra.RRA_FLOAT32) == rra.RRA_ALGO_ONE_SHOT
+    assert rra.rra_select_algo(1, 1 << 30, rra.RRA_FLOAT32) == rra.RRA_ALGO_ONE_SHOT
+    p = tmp_path / "tune.txt"
+    p.write_text("# n dtype log2_bytes algo\n8 float32 10 ring\n8 float32 20 two_shot\n"
+                 "8 float32 26 one_shot  # big\n4 int32 0 ring\n")
+    rra.rra_load_tuning(str(p))
+    assert rra.rra_select_algo(8, 1024, rra.RRA_FLOAT32) == rra.RRA_ALGO_RING
+    assert rra.rra_select_algo(8, (1 << 20) + 1, rra.RRA_FLOAT32) == rra.RRA_ALGO_TWO_SHOT
+    assert rra.rra_select_algo(8, 1 << 30, rra.RRA_FLOAT32) == rra.RRA_ALGO_ONE_SHOT
+    assert rra.rra_select_algo(4, 7, rra.RRA_INT32) == rra.RRA_ALGO_RING
+    bad = tmp_path / "bad.txt"
+    bad.write_text("8 float32 10 warp_drive\n")
+    assert rra.rra_load_tuning(str(bad), check=False) == rra.RRA_ERR_INVALID_ARG
+    assert rra.rra_select_algo(8, 1024, rra.RRA_FLOAT32) == rra.RRA_ALGO_RING  # old table kept
+    rra.rra_load_tuning(None)

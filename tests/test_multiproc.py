@@ -1,0 +1,66 @@
+"""The benchmark's multi-replica path on CPU: two gloo ranks, each a replica
+with its own time; the job takes the slowest rank's time and every rank's
+bytes."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    mine = [10.0 + rank, 100.0 - rank]  # rank 1 is slower in the first slot
+    got = bench.max_over_ranks(mine, dist, "cpu")
+    q.put((rank, got))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0] == res[1] == [11.0, 100.0]
+
+
+def test_job_throughput_counts_every_replica():
+    import bench
+
+    # 2 replicas x 1 GB per step x 10 steps in 1 s -> 20 GB/s
+    assert bench.job_throughput(1e9, 2, 10, 1000.0) == pytest.approx(20.0)
+    assert bench.max_over_ranks([1.0, 2.0], None, "cpu") == [1.0, 2.0]
+
+
+def test_floor_bytes_and_bus_factors():
+    import bench
+    from oracle import model
+
+    S = 100
+    assert bench.floor_bytes("ar_ring", 8, S) == 1600
+    assert bench.floor_bytes("rs_direct", 8, S) == 900
+    assert bench.floor_bytes("ag_ring", 8, S) == 900
+    # the bench's bus factors are the page's (pinned in the oracle tests)
+    assert bench.bus_factor("ar_x", 8) == model.bus_factor("allreduce", 8)
+    assert bench.bus_factor("rs_x", 8) == model.bus_factor("reducescatter", 8)
+    assert bench.bus_factor("ag_x", 8) == model.bus_factor("allgather", 8)

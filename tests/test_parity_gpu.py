@@ -1,0 +1,309 @@
+"""GPU path vs the CPU oracle, element by element, through the C ABI.
+
+The bar: bit-exact for int32 and for float32 (the kernels sum in the
+oracle's order), and for bfloat16 the 1e-2 relative bound (with float32
+accumulation in the same order the results are expected bit-exact too, and
+the tests check both).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import collective_all_reduce_rank_gb300 as rra
+from collective_all_reduce_rank_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+AR = {"ring": rra.RRA_ALGO_RING, "oneshot": rra.RRA_ALGO_ONE_SHOT, "twoshot": rra.RRA_ALGO_TWO_SHOT}
+RSAG = {"ring": rra.RRA_ALGO_RING, "direct": rra.RRA_ALGO_DIRECT}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _init():
+    import torch
+
+    torch.cuda.set_device(0)
+    rra.rra_init(0)
+    rra.rra_set_timeout_ns(2_000_000_000)
+    yield
+
+
+def G():
+    import gpu_util
+
+    return gpu_util
+
+
+def _check(got, want, dtype, what):
+    g = G()
+    if dtype == "bfloat16":
+        assert g.bf16_rel_ok(got, want), what
+    g.assert_bits_equal(got, want, what)
+
+
+def _status_ok():
+    st, info = rra.rra_query_status()
+    assert st == rra.RRA_SUCCESS, info
+
+
+def run_allreduce(xs, dtype, algo, inplace=False, offset=0):
+    g = G()
+    n, count = len(xs), xs[0].size
+    if offset:
+        # element-aligned but not 16-byte aligned buffers: the element path
+        big = [g.to_dev(np.concatenate([np.zeros(offset, x.dtype), x]), dtype) for x in xs]
+        ins = [b[offset:] for b in big]
+        outs_big = g.empty(n, count + offset, dtype)
+        outs = [o[offset:] for o in outs_big]
+    else:
+        ins = [g.to_dev(x, dtype) for x in xs]
+        outs = ins if inplace else g.empty(n, count, dtype)
+    rra.rra_allreduce(ins, outs, count, g.CODE[dtype], rra.RRA_SUM, AR[algo])
+    _status_ok()
+    return [g.to_host(o, dtype) for o in outs]
+
+
+# --------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("algo", list(AR))
+@pytest.mark.parametrize("n", [2, 4, 8])
+@pytest.mark.parametrize("dtype", ["float32", "int32", "bfloat16"])
+def test_all_ones_sanity(algo, n, dtype):
+    xs = inputs.make_ranks(n, 128, dtype, "ones")
+    got = run_allreduce(xs, dtype, algo)
+    want, _, _ = oracle.allreduce(algo, xs, dtype)
+    for r in range(n):
+        _check(got[r], want[r], dtype, "ones r=%d" % r)
+        vals = G().bf16_bits_to_f64(got[r]) if dtype == "bfloat16" else got[r]
+        assert np.all(vals == n)
+
+
+@pytest.mark.parametrize("algo", list(AR))
+def test_small_exact_config(algo):
+    # n=2, float32 integers in [-8, 8], 4096 per rank
+    xs = inputs.cfg_small_exact()
+    got = run_allreduce(xs, "float32", algo)
+    want, _, _ = oracle.allreduce(algo, xs, "float32")
+    for r in range(2):
+        _check(got[r], want[r], "float32", "r=%d" % r)
+
+
+@pytest.mark.parametrize("algo", list(RSAG))
+def test_small_exact_config_rs_ag(algo):
+    g = G()
+    xs = inputs.cfg_small_exact()
+    ins = [g.to_dev(x, "float32") for x in xs]
+    outs = g.empty(2, 2048, "float32")
+    rra.rra_reduce_scatter(ins, outs, 2048, rra.RRA_FLOAT32, rra.RRA_SUM, RSAG[algo])
+    _status_ok()
+    want, _, _ = oracle.reduce_scatter(algo, xs, "float32")
+    for r in range(2):
+        _check(g.to_host(outs[r], "float32"), want[r], "float32", "rs r=%d" % r)
+    shards = [x[:2048].copy() for x in xs]
+    ins = [g.to_dev(x, "float32") for x in shards]
+    outs = g.empty(2, 4096, "float32")
+    rra.rra_all_gather(ins, outs, 2048, rra.RRA_FLOAT32, RSAG[algo])
+    _status_ok()
+    want, _, _ = oracle.all_gather(algo, shards, "float32")
+    for r in range(2):
+        _check(g.to_host(outs[r], "float32"), want[r], "float32", "ag r=%d" % r)
+
+
+@pytest.mark.parametrize("algo", list(AR))
+@pytest.mark.parametrize("tokens", inputs.TP_TOKENS)
+def test_tp_activations_bf16(algo, tokens):
+    xs = inputs.cfg_tp_activations(tokens)
+    got = run_allreduce(xs, "bfloat16", algo)
+    want, _, _ = oracle.allreduce(algo, xs, "bfloat16")
+    for r in range(8):
+        _check(got[r], want[r], "bfloat16", "tokens=%d r=%d" % (tokens, r))
+
+
+@pytest.mark.parametrize("algo", list(AR))
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_order_sensitive_float_data(algo, dtype, n):
+    # several tiles and channels, plus a ragged tail
+    count = 3 * 1024 * 16 * n + 7 * 8 + 3
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=21 + n, sigma=1e-2 if dtype == "float32" else 1.0)
+    got = run_allreduce(xs, dtype, algo)
+    want, _, _ = oracle.allreduce(algo, xs, dtype)
+    for r in range(n):
+        _check(got[r], want[r], dtype, "%s n=%d r=%d" % (algo, n, r))
+
+
+@pytest.mark.parametrize("algo", list(AR))
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("count", [1, 3, 4, 5, 8, 9, 17, 31, 100, 1001, 65537])
+def test_ragged_counts(algo, n, count):
+    xs = inputs.make_ranks(n, count, "float32", "normal", seed=count + n)
+    got = run_allreduce(xs, "float32", algo)
+    want, _, _ = oracle.allreduce(algo, xs, "float32")
+    for r in range(n):
+        _check(got[r], want[r], "float32", "n=%d count=%d r=%d" % (n, count, r))
+
+
+@pytest.mark.parametrize("algo", list(AR))
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_unaligned_element_path(algo, dtype):
+    n, count = 4, 10_000 + 3
+    xs = inputs.make_ranks(n, count, dtype, "normal", seed=5)
+    got = run_allreduce(xs, dtype, algo, offset=1)
+    want, _, _ = oracle.allreduce(algo, xs, dtype)
+    for r in range(n):
+        _check(got[r], want[r], dtype, "offset r=%d" % r)
+
+
+@pytest.mark.parametrize("algo", list(AR))
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+def test_in_place(algo, dtype):
+    n, count = 8, 200_003
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=8)
+    got = run_allreduce(xs, dtype, algo, inplace=True)
+    want, _, _ = oracle.allreduce(algo, xs, dtype)
+    for r in range(n):
+        _check(got[r], want[r], dtype, "inplace r=%d" % r)
+
+
+def test_world_size_one_and_empty():
+    g = G()
+    xs = inputs.make_ranks(1, 1000, "float32", "normal")
+    for algo in AR.values():
+        assert run_allreduce(xs, "float32", [k for k, v in AR.items() if v == algo][0])[0].tobytes() == xs[0].tobytes()
+    # count 0: success, no launch, outputs untouched
+    ins = [g.to_dev(np.ones(4, np.float32), "float32") for _ in range(2)]
+    outs = g.empty(2, 4, "float32", fill=7)
+    rra.rra_allreduce(ins, outs, 0, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_RING)
+    assert np.all(g.to_host(outs[0], "float32").view(np.int32) == 7)
+
+
+@pytest.mark.parametrize("algo", list(RSAG))
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n,rc", [(2, 2048), (3, 1001), (8, 5000), (8, 3), (5, 64 * 1024 + 1)])
+def test_reduce_scatter_and_all_gather(algo, dtype, n, rc):
+    g = G()
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, n * rc, dtype, dist, seed=rc)
+    ins = [g.to_dev(x, dtype) for x in xs]
+    outs = g.empty(n, rc, dtype)
+    rra.rra_reduce_scatter(ins, outs, rc, g.CODE[dtype], rra.RRA_SUM, RSAG[algo])
+    _status_ok()
+    want, _, _ = oracle.reduce_scatter(algo, xs, dtype)
+    for r in range(n):
+        _check(g.to_host(outs[r], dtype), want[r], dtype, "rs r=%d" % r)
+    shards = [x[:rc].copy() for x in xs]
+    ins = [g.to_dev(x, dtype) for x in shards]
+    outs = g.empty(n, n * rc, dtype)
+    rra.rra_all_gather(ins, outs, rc, g.CODE[dtype], RSAG[algo])
+    _status_ok()
+    want, _, _ = oracle.all_gather(algo, shards, dtype)
+    for r in range(n):
+        _check(g.to_host(outs[r], dtype), want[r], dtype, "ag r=%d" % r)
+
+
+@pytest.mark.parametrize("algo", list(RSAG))
+def test_rs_ag_in_place(algo):
+    import torch
+
+    g = G()
+    n, rc = 4, 10_000
+    xs = inputs.make_ranks(n, n * rc, "float32", "normal", seed=3)
+    ins = [g.to_dev(x, "float32") for x in xs]
+    outs = [t[r * rc:(r + 1) * rc] for r, t in enumerate(ins)]
+    rra.rra_reduce_scatter(ins, outs, rc, rra.RRA_FLOAT32, rra.RRA_SUM, RSAG[algo])
+    _status_ok()
+    want, _, _ = oracle.reduce_scatter(algo, xs, "float32")
+    for r in range(n):
+        _check(g.to_host(outs[r], "float32"), want[r], "float32", "rs in place r=%d" % r)
+    bufs = [torch.zeros(n * rc, dtype=torch.float32, device="cuda") for _ in range(n)]
+    shards = [x[:rc].copy() for x in xs]
+    for r in range(n):
+        bufs[r][r * rc:(r + 1) * rc] = g.to_dev(shards[r], "float32")
+    ins = [bufs[r][r * rc:(r + 1) * rc] for r in range(n)]
+    rra.rra_all_gather(ins, bufs, rc, rra.RRA_FLOAT32, RSAG[algo])
+    _status_ok()
+    want, _, _ = oracle.all_gather(algo, shards, "float32")
+    for r in range(n):
+        _check(g.to_host(bufs[r], "float32"), want[r], "float32", "ag in place r=%d" % r)
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n", [2, 4, 8])
+def test_ring_equals_rs_then_ag_on_gpu(dtype, n):
+    g = G()
+    rc = 4 * 1024 * 9
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, n * rc, dtype, dist, seed=77)
+    ar = run_allreduce(xs, dtype, "ring")
+    ins = [g.to_dev(x, dtype) for x in xs]
+    mid = g.empty(n, rc, dtype)
+    rra.rra_reduce_scatter(ins, mid, rc, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_RING)
+    outs = g.empty(n, n * rc, dtype)
+    rra.rra_all_gather(mid, outs, rc, g.CODE[dtype], rra.RRA_ALGO_RING)
+    _status_ok()
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], dtype), ar[r], "ring vs rs+ag r=%d" % r)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("algo", list(AR))
+def test_gradient_bucket_full_size(algo):
+    # n=8, float32 normal(0, 1e-2), 25M elements per rank (100 MB): the full
+    # workload the benchmark times, compared element by element.
+    xs = inputs.cfg_gradient_bucket()
+    got = run_allreduce(xs, "float32", algo)
+    want, _, _ = oracle.allreduce(algo, xs, "float32")
+    for r in range(8):
+        _check(got[r], want[r], "float32", "bucket r=%d" % r)
+
+
+def test_auto_and_repeat_calls_are_stable():
+    # many calls in a row: the per-call epoch keeps the step flags apart
+    g = G()
+    n, count = 8, 300_000
+    xs = inputs.make_ranks(n, count, "float32", "normal", seed=9)
+    ins = [g.to_dev(x, "float32") for x in xs]
+    want = {a: oracle.allreduce(a, xs, "float32")[0] for a in AR}
+    for rep in range(5):
+        for a, code in AR.items():
+            outs = g.empty(n, count, "float32")
+            rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, code)
+            _status_ok()
+            for r in (0, n - 1):
+                g.assert_bits_equal(g.to_host(outs[r], "float32"), want[a][r], "%s rep %d" % (a, rep))
+    outs = g.empty(n, count, "float32")
+    rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_AUTO)
+    _status_ok()
+    pick = rra.rra_select_algo(n, count * 4, rra.RRA_FLOAT32)
+    name = {v: k for k, v in AR.items()}[pick]
+    g.assert_bits_equal(g.to_host(outs[3], "float32"), want[name][3], "auto")
+
+
+def test_cuda_graph_capture():
+    import torch
+
+    g = G()
+    n, count = 4, 50_000
+    xs = inputs.make_ranks(n, count, "float32", "normal", seed=10)
+    ins = [g.to_dev(x, "float32") for x in xs]
+    outs = g.empty(n, count, "float32")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TWO_SHOT, stream=s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for a in (rra.RRA_ALGO_RING, rra.RRA_ALGO_TWO_SHOT, rra.RRA_ALGO_ONE_SHOT):
+            rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, a, stream=s)
+    want, _, _ = oracle.allreduce("oneshot", xs, "float32")
+    for rep in range(3):
+        for o in outs:
+            o.fill_(0)
+        graph.replay()
+        torch.cuda.synchronize()
+        _status_ok()
+        for r in range(n):
+            g.assert_bits_equal(g.to_host(outs[r], "float32"), want[r], "graph replay %d" % rep)
