@@ -374,7 +374,7 @@ def run_ours(args):
         "parity_sample_ok": parity,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_scale)
+        line["cpu_baseline"] = cpu_baseline(args.cpu_scale or 2)
     if args.small:
         line["tp_latency_us"] = tp_latency(torch, rra, inputs, stream)
     print(json.dumps(line), flush=True)
@@ -468,12 +468,26 @@ def cpu_baseline(scale):
                       "single-threaded C oracle" % (scale, BUCKET // scale, LL_BYTES // scale)}
 
 
+FULL_STEP_CPU_S = 26.0  # one oracle step at full size on one core, measured
+
+
+def reference_scale(steps, warmup, budget_s=120.0):
+    """Sample fraction (a power of two, at least 1/4) that keeps the whole
+    reference run near `budget_s` seconds of CPU work."""
+    scale = 4
+    while (steps + warmup) * FULL_STEP_CPU_S / scale > budget_s and scale < 1024:
+        scale *= 2
+    return scale
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     import oracle
 
+    if args.cpu_scale is None:
+        args.cpu_scale = reference_scale(args.steps, args.warmup)
     host = sample_host(args.cpu_scale)
     for k in range(args.warmup):
         oracle_step(oracle, host, k + 1)
@@ -629,13 +643,46 @@ def time_call(torch, call, stream, total_bytes):
     return statistics.median(samples)
 
 
+def run_profile(args):
+    """Run the listed operations once each on a 1/scale workload (the small
+    case the ncu captures use); exits non-zero on a device error."""
+    import torch
+
+    import collective_all_reduce_rank_gb300 as rra
+    from collective_all_reduce_rank_gb300 import inputs
+
+    torch.cuda.set_device(0)
+    rra.rra_init(0)
+    step = Step(torch, rra, inputs, seed=0, scale=args.scale)
+    stream = torch.cuda.Stream()
+    names = [o[0] for o in step.ops] if args.profile == "all" else args.profile.split(",")
+    step.flag = 1
+    with torch.cuda.stream(stream):
+        for name in names:
+            if name == "ll_unpack" and "ll_pack" not in names:
+                step.run_op("ll_pack", stream)
+            if name == "ll128_unpack" and "ll128_pack" not in names:
+                step.run_op("ll128_pack", stream)
+            step.run_op(name, stream)
+    torch.cuda.synchronize()
+    st, info = rra.rra_query_status(stream)
+    if st != 0:
+        raise SystemExit("device status %d %s" % (st, info))
+    print(json.dumps({"profile": names, "scale": args.scale, "bucket_elems_per_rank": step.count,
+                      "ll_payload_bytes": step.llb}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-scale", type=int, default=4, help="oracle sample = 1/scale of the workload")
+    ap.add_argument("--cpu-scale", type=int, default=None,
+                    help="oracle sample = 1/scale of the workload (default: 2 for the CPU baseline, "
+                         "sized to the step count for --impl reference)")
+    ap.add_argument("--profile", default=None, help="run these ops once (comma list or 'all') and exit")
+    ap.add_argument("--scale", type=int, default=4, help="workload fraction for --profile")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true", help="add the TP-activation latency table")
     ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")
@@ -645,6 +692,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.profile:
+        run_profile(args)
     elif args.sweep:
         run_sweep(args)
     else:

@@ -39,6 +39,7 @@ RRA_ALGO_RING = 1
 RRA_ALGO_ONE_SHOT = 2
 RRA_ALGO_TWO_SHOT = 3
 RRA_ALGO_DIRECT = 4
+RRA_ALGO_COPY_ENGINE = 5
 
 RRA_MAX_RANKS = 8
 
@@ -87,6 +88,7 @@ def _declare(lib):
         "rra_allreduce": (i, [vpp, vpp, i, sz, i, i, i, vp]),
         "rra_reduce_scatter": (i, [vpp, vpp, i, sz, i, i, i, vp]),
         "rra_all_gather": (i, [vpp, vpp, i, sz, i, i, vp]),
+        "rra_allreduce_rmsnorm": (i, [vpp, vpp, i, sz, sz, vp, ctypes.c_float, i, vp]),
         "rra_ll_wire_bytes": (sz, [sz]),
         "rra_ll128_wire_bytes": (sz, [sz]),
         "rra_ll_pack": (i, [vp, sz, vp, u32, vp]),
@@ -98,6 +100,7 @@ def _declare(lib):
         "rra_load_tuning": (i, [ctypes.c_char_p]),
         "rra_set_timeout_ns": (None, [u64]),
         "rra_debug_skip_rank": (None, [i]),
+        "rra_set_max_ctas": (None, [i]),
         "rra_status_string": (ctypes.c_char_p, [i]),
         "rra_dump_recent": (i, [ctypes.c_char_p, sz]),
     }
@@ -220,6 +223,16 @@ def rra_all_gather(bufs, outs, sendcount=None, dtype=None, algo=RRA_ALGO_AUTO, s
     return _ret(st, "rra_all_gather", check)
 
 
+def rra_allreduce_rmsnorm(bufs, outs, gamma, hidden, eps=1e-6, rows=None, dtype=None, stream=None,
+                          check=True, nranks=None) -> int:
+    count, dtype = _resolve(bufs, None if rows is None else rows * hidden, dtype)
+    rows = count // hidden if rows is None else rows
+    n = len(bufs) if nranks is None else nranks
+    st = load().rra_allreduce_rmsnorm(_ptr_array(bufs), _ptr_array(outs), n, rows, hidden, _ptr(gamma),
+                                      eps, dtype, _stream(stream, bufs[0] if bufs else None))
+    return _ret(st, "rra_allreduce_rmsnorm", check)
+
+
 def rra_ll_wire_bytes(payload_bytes: int) -> int:
     return int(load().rra_ll_wire_bytes(payload_bytes))
 
@@ -287,6 +300,10 @@ def rra_set_timeout_ns(ns: int) -> None:
 
 def rra_debug_skip_rank(rank: int) -> None:
     load().rra_debug_skip_rank(rank)
+
+
+def rra_set_max_ctas(max_ctas: int) -> None:
+    load().rra_set_max_ctas(max_ctas)
 
 
 def rra_dump_recent() -> str:

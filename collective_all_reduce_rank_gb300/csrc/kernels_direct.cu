@@ -142,7 +142,9 @@ static int occupancy_of(Kern k) {
 
 static int grid_for(size_t units, int occ, int rows) {
   const size_t want = (units + kDirectThreads - 1) / kDirectThreads;
-  const size_t cap = (size_t)std::max(1, device_sms() * occ / rows);
+  int per_row = std::max(1, device_sms() * occ / rows);
+  if (max_ctas_cap() > 0) per_row = std::max(1, std::min(per_row, max_ctas_cap() / rows));
+  const size_t cap = (size_t)per_row;
   return (int)std::max<size_t>(1, std::min(want, cap));
 }
 

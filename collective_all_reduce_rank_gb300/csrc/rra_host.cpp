@@ -38,6 +38,7 @@ DevState g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 std::atomic<uint64_t> g_timeout_ns{0};
 std::atomic<int> g_skip_rank{-1};
+std::atomic<int> g_max_ctas{-1};  // -1: not set, read RRA_MAX_CTAS
 
 // ---------------------------------------------------------------------------
 // environment
@@ -62,6 +63,12 @@ uint64_t timeout_ns() {
   return env ? env : kDefaultTimeoutNs;
 }
 
+// Channels per rank the SM budget leaves a persistent kernel.
+long channel_cap(int n) {
+  const int m = rra::max_ctas_cap();
+  return m > 0 ? std::max(1, m / n) : (long)kMaxChannels;
+}
+
 size_t elem_size(rra_dtype_t dt) { return dt == RRA_BFLOAT16 ? 2 : 4; }
 
 const char* dtype_name(int dt) {
@@ -75,6 +82,7 @@ const char* algo_name(int a) {
     case RRA_ALGO_ONE_SHOT: return "one_shot";
     case RRA_ALGO_TWO_SHOT: return "two_shot";
     case RRA_ALGO_DIRECT: return "direct";
+    case RRA_ALGO_COPY_ENGINE: return "copy_engine";
     default: return "?";
   }
 }
@@ -222,7 +230,8 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   const size_t units0 = (a.chunk_len[0] + pu - 1) / pu;
   const size_t need = (units0 + a.tile_units - 1) / a.tile_units;
-  long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need)});
+  long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
+                           channel_cap(n)});
   c = std::min(c, env_long("RRA_TWOSHOT_CHANNELS", c));
   if (c < 1) return RRA_ERR_UNSUPPORTED;
   a.channels = (int)c;
@@ -265,7 +274,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   const size_t need = (maxu + (size_t)a.G * a.slice_units - 1) / ((size_t)a.G * a.slice_units);
   const size_t fifo_cap = s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes);
   long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
-                           (long)fifo_cap, env_long("RRA_RING_CHANNELS", 16)});
+                           (long)fifo_cap, env_long("RRA_RING_CHANNELS", 16), channel_cap(n)});
   if (c < 1) return RRA_ERR_UNSUPPORTED;
   a.channels = (int)c;
   a.fifo = s->ws.fifo;
@@ -283,6 +292,15 @@ bool all_aligned16(const void* const* p, int n) {
 }
 
 }  // namespace
+
+int rra::max_ctas_cap() {
+  int m = g_max_ctas.load();
+  if (m < 0) {
+    static const int env = (int)env_long("RRA_MAX_CTAS", 0);
+    m = env > 0 ? env : 0;
+  }
+  return m;
+}
 
 // ===========================================================================
 // C ABI
@@ -347,6 +365,8 @@ rra_status_t rra_finalize(int device) {
 }
 
 void rra_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
+
+void rra_set_max_ctas(int max_ctas) { g_max_ctas.store(max_ctas < 0 ? 0 : max_ctas); }
 
 void rra_debug_skip_rank(int rank) { g_skip_rank.store(rank); }
 
@@ -455,6 +475,26 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
     }
     a.count = count;
     a.per_rank_grid = (int)env_long("RRA_ONESHOT_PER_RANK", 0) != 0;
+    if (vec && !a.per_rank_grid && env_long("RRA_ONESHOT_TMA", 0) != 0 && count * e >= 16) {
+      // whole 16-byte units by bulk copies, the sub-unit tail by the LSU kernel
+      const size_t units = count * e / 16;
+      DevState* s = current_state(nullptr);
+      DevStatus* status = (s && s->ready) ? s->ws.status : nullptr;
+      int grid = 0;
+      cudaError_t err = launch_oneshot_tma(nranks, dtype, bufs, outs, units, status, timeout_ns(), &grid, st);
+      const size_t done = units * 16 / e;
+      if (err == cudaSuccess && done < count) {
+        DirectArgs t{};
+        for (int r = 0; r < nranks; ++r) {
+          t.in[r] = static_cast<const char*>(bufs[r]) + done * e;
+          t.out[r] = static_cast<char*>(outs[r]) + done * e;
+        }
+        t.count = count - done;
+        int g2 = 0;
+        err = launch_oneshot(nranks, dtype, false, t, 1, &g2, st);
+      }
+      return record(call, algo, nranks, count, dtype, grid, cuda_status(err));
+    }
     int grid = 0;
     const cudaError_t err = launch_oneshot(nranks, dtype, vec, a, (count * e + 15) / 16, &grid, st);
     return record(call, algo, nranks, count, dtype, grid, cuda_status(err));
@@ -549,7 +589,7 @@ rra_status_t rra_all_gather(const void* const* bufs, void* const* outs, int nran
                             rra_dtype_t dtype, rra_algo_t algo, rra_stream_t stream) {
   const char* call = "all_gather";
   if (!bufs || !outs || nranks < 1 || !valid_dtype(dtype) || (int)algo < 0 ||
-      (int)algo > RRA_ALGO_DIRECT || algo == RRA_ALGO_ONE_SHOT)
+      (int)algo > RRA_ALGO_COPY_ENGINE || algo == RRA_ALGO_ONE_SHOT)
     return record(call, algo, nranks, sendcount, dtype, 0,
                   nranks > kMaxRanks ? RRA_ERR_UNSUPPORTED : RRA_ERR_INVALID_ARG);
   if (nranks > kMaxRanks) return record(call, algo, nranks, sendcount, dtype, 0, RRA_ERR_UNSUPPORTED);
@@ -572,6 +612,18 @@ rra_status_t rra_all_gather(const void* const* bufs, void* const* outs, int nran
   if (algo == RRA_ALGO_AUTO || algo == RRA_ALGO_TWO_SHOT) algo = RRA_ALGO_DIRECT;
   if (sendcount == 0) return record(call, algo, nranks, sendcount, dtype, 0, RRA_SUCCESS);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (algo == RRA_ALGO_COPY_ENGINE) {
+    // one device-to-device copy per (destination, shard); the shard already
+    // in place is skipped
+    cudaError_t err = cudaSuccess;
+    for (int r = 0; r < nranks && err == cudaSuccess; ++r)
+      for (int q = 0; q < nranks && err == cudaSuccess; ++q) {
+        char* dst = static_cast<char*>(outs[r]) + (size_t)q * sbytes;
+        if (dst == bufs[q]) continue;
+        err = cudaMemcpyAsync(dst, bufs[q], sbytes, cudaMemcpyDeviceToDevice, st);
+      }
+    return record(call, algo, nranks, sendcount, dtype, 0, cuda_status(err));
+  }
   const bool vec = all_aligned16(bufs, nranks) && all_aligned16((const void* const*)outs, nranks) &&
                    (sbytes % 16) == 0;
   if (algo == RRA_ALGO_DIRECT || nranks == 1) {
@@ -597,6 +649,37 @@ rra_status_t rra_all_gather(const void* const* bufs, void* const* outs, int nran
   const rra_status_t rs =
       run_ring(s, bufs, outs, nranks, kRingAllGather, ib, ob, len, dtype, vec, st, &grid);
   return record(call, algo, nranks, sendcount, dtype, grid, rs);
+}
+
+rra_status_t rra_allreduce_rmsnorm(const void* const* bufs, void* const* outs, int nranks,
+                                   size_t rows, size_t hidden, const void* gamma, float eps,
+                                   rra_dtype_t dtype, rra_stream_t stream) {
+  const char* call = "allreduce_rmsnorm";
+  const size_t count = rows * hidden;
+  if (!bufs || !outs || !gamma || nranks < 1 || (dtype != RRA_FLOAT32 && dtype != RRA_BFLOAT16) ||
+      hidden == 0 || !(eps >= 0.f))
+    return record(call, RRA_ALGO_ONE_SHOT, nranks, count, dtype, 0,
+                  nranks > kMaxRanks ? RRA_ERR_UNSUPPORTED : RRA_ERR_INVALID_ARG);
+  if (nranks > kMaxRanks || hidden > kNormMaxHidden || rows > 0x7FFFFFFFull)
+    return record(call, RRA_ALGO_ONE_SHOT, nranks, count, dtype, 0, RRA_ERR_UNSUPPORTED);
+  const size_t e = elem_size(dtype);
+  if (rows && hidden > (SIZE_MAX / 4) / rows / e)
+    return record(call, RRA_ALGO_ONE_SHOT, nranks, count, dtype, 0, RRA_ERR_INVALID_ARG);
+  if (!aligned(gamma, e)) return record(call, RRA_ALGO_ONE_SHOT, nranks, count, dtype, 0, RRA_ERR_INVALID_ARG);
+  for (int r = 0; r < nranks; ++r)
+    if (!bufs[r] || !outs[r] || !aligned(bufs[r], e) || !aligned(outs[r], e))
+      return record(call, RRA_ALGO_ONE_SHOT, nranks, count, dtype, 0, RRA_ERR_INVALID_ARG);
+  const size_t S = count * e;
+  rra_status_t al = check_alias(bufs, S, outs, S, nranks, reinterpret_cast<const char* const*>(outs));
+  for (int r = 0; r < nranks && al == RRA_SUCCESS; ++r)
+    if (overlap(outs[r], S, gamma, hidden * e)) al = RRA_ERR_ALIAS;
+  if (al != RRA_SUCCESS) return record(call, RRA_ALGO_ONE_SHOT, nranks, count, dtype, 0, al);
+  if (rows == 0) return record(call, RRA_ALGO_ONE_SHOT, nranks, 0, dtype, 0, RRA_SUCCESS);
+  const bool vec = all_aligned16(bufs, nranks) && all_aligned16((const void* const*)outs, nranks) &&
+                   aligned(gamma, 16) && (hidden * e) % 16 == 0;
+  const cudaError_t err = launch_allreduce_rmsnorm(nranks, dtype, vec, bufs, outs, gamma, rows, hidden, eps,
+                                                   reinterpret_cast<cudaStream_t>(stream));
+  return record(call, RRA_ALGO_ONE_SHOT, nranks, count, dtype, (int)rows, cuda_status(err));
 }
 
 size_t rra_ll_wire_bytes(size_t payload_bytes) { return 8 * ((payload_bytes + 3) / 4); }

@@ -133,6 +133,10 @@ constexpr int kRingUnitsPerThread = 2;
 constexpr int kTwoShotUnitsPerThread = 2;
 constexpr int kLLThreads = 256;
 
+// SM budget set by rra_set_max_ctas (0: none); kernels_direct.cu caps its
+// grids with it.
+int max_ctas_cap();
+
 // Streaming kernels: `units` 16-byte units per grid row; *grid receives the
 // CTAs per row launched.
 cudaError_t launch_oneshot(int n, int dt, bool vec, const DirectArgs& a, size_t units, int* grid,
@@ -141,6 +145,17 @@ cudaError_t launch_direct_rs(int n, int dt, bool vec, const DirectArgs& a, size_
                              cudaStream_t s);
 cudaError_t launch_direct_ag(int n, int dt, bool vec, const DirectArgs& a, size_t units, int* grid,
                              cudaStream_t s);
+
+// One-shot with bulk-copy staging: whole 16-byte units only, 16-byte
+// aligned buffers; status may be null.
+cudaError_t launch_oneshot_tma(int n, int dt, const void* const* in, void* const* out, size_t units,
+                               DevStatus* status, uint64_t timeout_ns, int* grid, cudaStream_t s);
+
+// All-reduce + RMSNorm, one CTA per row (hidden <= kNormMaxHidden).
+constexpr size_t kNormMaxHidden = 51200;
+cudaError_t launch_allreduce_rmsnorm(int n, int dt, bool vec, const void* const* in, void* const* out,
+                                     const void* gamma, size_t rows, size_t hidden, float eps,
+                                     cudaStream_t s);
 
 // Persistent kernels are launched cooperatively: every CTA is resident or
 // the launch fails.  *max_blocks_per_sm reports the occupancy limit.

@@ -79,7 +79,11 @@ typedef enum {
   RRA_ALGO_RING = 1,
   RRA_ALGO_ONE_SHOT = 2,
   RRA_ALGO_TWO_SHOT = 3,
-  RRA_ALGO_DIRECT = 4
+  RRA_ALGO_DIRECT = 4,
+  /** all-gather only: the GPU's copy engines move the shards
+   *  (cudaMemcpyAsync device to device), no SM runs a kernel ([AIH]
+   *  "Protocols": transfer methods that use no SMs, like the copy engine). */
+  RRA_ALGO_COPY_ENGINE = 5
 } rra_algo_t;
 
 /* ------------------------------------------------------------------------ */
@@ -143,12 +147,31 @@ rra_status_t rra_reduce_scatter(const void* const* bufs, void* const* outs, int 
  *  holds nranks*sendcount: outs[r][q*sendcount + i] = bufs[q][i].
  *  - algo RING: the ring's all-gather half (n-1 forwarding steps).
  *    DIRECT/TWO_SHOT/AUTO: every rank reads every shard directly.
+ *    COPY_ENGINE: nranks^2 device-to-device copies on `stream` (no kernel).
  *  - In place: bufs[r] == outs[r] + r*sendcount elements for every r.
  *  The data are copied bit for bit, whatever dtype says.
  *  Errors as rra_allreduce; ONE_SHOT is RRA_ERR_INVALID_ARG. */
 rra_status_t rra_all_gather(const void* const* bufs, void* const* outs, int nranks,
                             size_t sendcount, rra_dtype_t dtype, rra_algo_t algo,
                             rra_stream_t stream);
+
+/** All-reduce fused with RMSNorm ([AIH] "Source code": FlashInfer's fused
+ *  all-reduce + RMSNorm for tensor-parallel activations).  bufs[r] and
+ *  outs[r] hold rows x hidden elements, row-major.  Every rank gets
+ *  outs[r][i][j] = s[i][j] * rsqrt(mean_j(s[i][j]^2) + eps) * gamma[j],
+ *  where s = SUM_k bufs[k] summed in float32 in ascending rank order (the
+ *  one-shot sum).  The normalisation runs in float32; the result is
+ *  rounded to dtype once.
+ *  - gamma: device pointer, hidden elements of dtype (must not overlap an
+ *    output).
+ *  - dtype: RRA_FLOAT32 or RRA_BFLOAT16; hidden in [1, 51200]; in place
+ *    (outs[r] == bufs[r]) allowed.
+ *  Errors: RRA_ERR_INVALID_ARG (int32, null, misaligned, hidden 0),
+ *  RRA_ERR_UNSUPPORTED (hidden > 51200, nranks > RRA_MAX_RANKS),
+ *  RRA_ERR_ALIAS, RRA_ERR_CUDA.  rows == 0 returns RRA_SUCCESS. */
+rra_status_t rra_allreduce_rmsnorm(const void* const* bufs, void* const* outs, int nranks,
+                                   size_t rows, size_t hidden, const void* gamma, float eps,
+                                   rra_dtype_t dtype, rra_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* LL and LL128 wire formats ([AIH] "Protocols")                            */
@@ -230,6 +253,14 @@ rra_status_t rra_load_tuning(const char* path);
  *  (ring and two-shot step flags, LL/LL128 line flags).  Default 500 ms
  *  or RRA_TIMEOUT_NS from the environment; 0 restores the default. */
 void rra_set_timeout_ns(uint64_t ns);
+
+/** SM budget ([AIH] "Protocols": each channel is a CUDA block, and
+ *  communication kernels compete with compute for SMs): at most
+ *  `max_ctas` CTAs per launch (0 = no limit, the default, or RRA_MAX_CTAS
+ *  from the environment).  Streaming kernels shrink their grid and loop
+ *  longer; ring and two-shot use at most max_ctas / nranks channels (at
+ *  least one). */
+void rra_set_max_ctas(int max_ctas);
 
 /** Fault injection for tests: virtual rank `rank` posts no step flag in the
  *  following ring and two-shot calls (-1 turns it off), so its peers' waits

@@ -40,7 +40,7 @@ def build(force: bool = False) -> str:
         if force or stale:
             tmp = _LIB + ".%d.tmp" % os.getpid()
             cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-                   "-Wall", "-fPIC", "-shared", "-o", tmp, _SRC]
+                   "-Wall", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
             subprocess.check_call(cmd)
             os.replace(tmp, _LIB)
     return _LIB
@@ -77,6 +77,9 @@ def _load():
     lib.orc_ll128_unpack.restype = ctypes.c_longlong
     lib.orc_ll128_unpack.argtypes = [vpp, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                      ctypes.c_int, ctypes.c_uint64]
+    lib.orc_allreduce_rmsnorm.restype = ctypes.c_int
+    lib.orc_allreduce_rmsnorm.argtypes = [ctypes.c_int, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int,
+                                          vpp, ctypes.c_void_p, ctypes.c_double, vpp]
     lib.orc_f32_to_bf16.restype = ctypes.c_uint16
     lib.orc_f32_to_bf16.argtypes = [ctypes.c_float]
     lib.orc_bf16_to_f32.restype = ctypes.c_float
@@ -151,6 +154,20 @@ def all_gather(algo: str, xs, dtype: str):
     if rc != 0:
         raise RuntimeError("oracle %s failed: %d" % (fn, rc))
     return outs, list(sent), list(recv)
+
+
+def allreduce_rmsnorm(xs, gamma, eps: float, dtype: str, hidden: int):
+    """Fused all-reduce + RMSNorm of rows of `hidden` elements: every rank
+    gets RMSNorm(sum_k xs[k]) * gamma.  Returns the n outputs."""
+    _check(list(xs) + [gamma], dtype)
+    n = len(xs)
+    rows = xs[0].size // hidden
+    outs = [np.zeros(xs[0].size, dtype=NP_DTYPES[dtype]) for _ in range(n)]
+    rc = _load().orc_allreduce_rmsnorm(n, rows, hidden, DTYPES[dtype], _ptrs(xs), gamma.ctypes.data,
+                                       eps, _ptrs(outs))
+    if rc != 0:
+        raise RuntimeError("oracle allreduce_rmsnorm failed: %d" % rc)
+    return outs
 
 
 def ll_wire_bytes(payload_bytes: int) -> int:

@@ -37,6 +37,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 
 #define ORC_INT32 0
 #define ORC_FLOAT32 1
@@ -538,4 +539,46 @@ long long orc_ll128_unpack(const void* const* wires, int nsrc, void* out, size_t
                            int dt, uint64_t expected_flag) {
   if (nsrc < 1 || payload_bytes % elem_size(dt)) return -2;
   return unpack_reduce(wires, nsrc, out, payload_bytes, dt, 128u, 120u, 8, expected_flag);
+}
+
+/* ------------------------------------------------------------------------ */
+/* fused all-reduce + RMSNorm                                               */
+/* ------------------------------------------------------------------------ */
+
+/* "Collective communication: NCCL's algorithms and protocols, ...",
+ * section "Source code", names FlashInfer's fused all-reduce + RMSNorm for
+ * the tensor-parallel activations [tokens, hidden]; the page gives no
+ * formula.  Reading taken: the all-reduce is the one-shot sum (float32,
+ * ascending rank order), then each row is normalised by its root mean
+ * square: y[i][j] = s[i][j] / sqrt(mean_j(s[i][j]^2) + eps) * gamma[j].
+ * The normalisation runs in double here (no precision is fixed for it) and
+ * the result is rounded to the element type once (float32 first, then
+ * bfloat16 for bfloat16 output).  Every rank receives the same rows.
+ * gamma has the element type; int32 is not accepted. */
+int orc_allreduce_rmsnorm(int n, size_t rows, size_t hidden, int dt, const void* const* in,
+                          const void* gamma, double eps, void* const* out) {
+  if (n < 1 || dt == ORC_INT32) return ORC_EINVAL;
+  float* s = (float*)malloc(hidden * 4 + 4);
+  float* g = (float*)malloc(hidden * 4 + 4);
+  float* y = (float*)malloc(hidden * 4 + 4);
+  if (!s || !g || !y) {
+    free(s);
+    free(g);
+    free(y);
+    return ORC_ENOMEM;
+  }
+  acc_load(dt, gamma, 0, hidden, g);
+  for (size_t i = 0; i < rows; ++i) {
+    acc_load(dt, in[0], i * hidden, hidden, s);
+    for (int k = 1; k < n; ++k) acc_add(dt, s, in[k], i * hidden, hidden);
+    double ss = 0.0;
+    for (size_t j = 0; j < hidden; ++j) ss += (double)s[j] * (double)s[j];
+    const double inv = 1.0 / sqrt(ss / (double)hidden + eps);
+    for (size_t j = 0; j < hidden; ++j) y[j] = (float)((double)s[j] * inv * (double)g[j]);
+    for (int r = 0; r < n; ++r) acc_store(dt, y, out[r], i * hidden, hidden);
+  }
+  free(s);
+  free(g);
+  free(y);
+  return ORC_OK;
 }

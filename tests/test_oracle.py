@@ -485,3 +485,55 @@ def test_crossover():
     assert model.oneshot_twoshot_crossover(2, 1.5e-6, 450e9) is None
     for S in (1e3, 1e6, 1e9):
         assert model.ab_time("one-shot", 2, S, 1.5e-6, 450e9) <= model.ab_time("two-shot", 2, S, 1.5e-6, 450e9)
+
+
+# --------------------------------------------------------------------------
+# fused all-reduce + RMSNorm
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+def test_rmsnorm_matches_torch_float64(dtype):
+    # library routine: torch's rms_norm in float64 on the float32 sums
+    import torch
+
+    n, rows, hidden, eps = 4, 6, 5120, 1e-6
+    xs = inputs.make_ranks(n, rows * hidden, dtype, "normal", seed=31)
+    gamma = inputs.make_ranks(1, hidden, dtype, "normal", seed=32)[0]
+    outs = oracle.allreduce_rmsnorm(xs, gamma, eps, dtype, hidden)
+    sums, _, _ = oracle.allreduce("oneshot", xs, dtype)
+    # the oracle's float32 sums, recovered exactly for float32; for bfloat16
+    # recompute them in float32 from the widened inputs (same order)
+    if dtype == "float32":
+        s = torch.from_numpy(sums[0].astype(np.float64)).view(rows, hidden)
+        g = torch.from_numpy(gamma.astype(np.float64))
+    else:
+        acc = np.zeros(rows * hidden, np.float32)
+        for x in xs:
+            acc = acc + oracle.bf16_to_f32(x)
+        s = torch.from_numpy(acc.astype(np.float64)).view(rows, hidden)
+        g = torch.from_numpy(oracle.bf16_to_f32(gamma).astype(np.float64))
+    want = torch.nn.functional.rms_norm(s, (hidden,), weight=g, eps=eps).reshape(-1).numpy()
+    for o in outs:
+        got = o.astype(np.float64) if dtype == "float32" else oracle.bf16_to_f32(o).astype(np.float64)
+        ulp = 2.0 ** -23 if dtype == "float32" else 2.0 ** -7
+        assert np.all(np.abs(got - want) <= ulp * np.abs(want) + 1e-30)
+    assert all(o.tobytes() == outs[0].tobytes() for o in outs)
+
+
+def test_rmsnorm_closed_forms():
+    # a row of equal sums c gives gamma * c / sqrt(c^2 + eps); eps = 0 -> gamma
+    n, hidden = 2, 64
+    xs = [np.full(2 * hidden, 1.5, np.float32), np.full(2 * hidden, 2.0, np.float32)]
+    gamma = np.linspace(-2, 2, hidden).astype(np.float32)
+    out = oracle.allreduce_rmsnorm(xs, gamma, 0.0, "float32", hidden)[0]
+    assert np.allclose(out, np.tile(gamma, 2), rtol=0, atol=2e-7)
+    out = oracle.allreduce_rmsnorm(xs, gamma, 3.0, "float32", hidden)[0]
+    want = gamma.astype(np.float64) * 3.5 / np.sqrt(3.5 ** 2 + 3.0)
+    assert np.allclose(out, np.tile(want, 2), rtol=1e-7, atol=0)
+    # scale invariance with eps = 0 and the unit mean square of the output
+    xs = inputs.make_ranks(3, 4 * hidden, "float32", "normal", seed=2)
+    a = oracle.allreduce_rmsnorm(xs, np.ones(hidden, np.float32), 0.0, "float32", hidden)[0]
+    b = oracle.allreduce_rmsnorm([x * 8 for x in xs], np.ones(hidden, np.float32), 0.0, "float32", hidden)[0]
+    assert np.array_equal(a, b)  # power-of-two scaling is exact
+    ms = (a.astype(np.float64).reshape(4, hidden) ** 2).mean(axis=1)
+    assert np.allclose(ms, 1.0, rtol=1e-6)

@@ -145,6 +145,23 @@ def test_ragged_counts(algo, n, count):
         _check(got[r], want[r], "float32", "n=%d count=%d r=%d" % (n, count, r))
 
 
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n", [1, 2, 3, 8])
+@pytest.mark.parametrize("count", [4, 4099, 5 * 2048 * 4 + 13, 1_000_003])
+def test_oneshot_bulk_copy_path(dtype, n, count, monkeypatch):
+    # the bulk-copy (TMA) staged one-shot: same bits as the oracle's one-shot
+    monkeypatch.setenv("RRA_ONESHOT_TMA", "1")
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=count + 7 * n)
+    got = run_allreduce(xs, dtype, "oneshot")
+    want, _, _ = oracle.allreduce("oneshot", xs, dtype)
+    for r in range(n):
+        _check(got[r], want[r], dtype, "tma n=%d count=%d r=%d" % (n, count, r))
+    got = run_allreduce(xs, dtype, "oneshot", inplace=True)
+    for r in range(n):
+        _check(got[r], want[r], dtype, "tma in place r=%d" % r)
+
+
 @pytest.mark.parametrize("algo", list(AR))
 @pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
 def test_unaligned_element_path(algo, dtype):
@@ -202,6 +219,47 @@ def test_reduce_scatter_and_all_gather(algo, dtype, n, rc):
     want, _, _ = oracle.all_gather(algo, shards, dtype)
     for r in range(n):
         _check(g.to_host(outs[r], dtype), want[r], dtype, "ag r=%d" % r)
+
+
+@pytest.mark.parametrize("n,sc", [(2, 100), (8, 5000), (8, 3)])
+def test_all_gather_copy_engine(n, sc):
+    import torch
+
+    g = G()
+    shards = inputs.make_ranks(n, sc, "int32", "bits", seed=sc)
+    ins = [g.to_dev(x, "int32") for x in shards]
+    outs = g.empty(n, n * sc, "int32")
+    rra.rra_all_gather(ins, outs, sc, rra.RRA_INT32, rra.RRA_ALGO_COPY_ENGINE)
+    _status_ok()
+    want, _, _ = oracle.all_gather("direct", shards, "int32")
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], "int32"), want[r], "copy engine r=%d" % r)
+    # in place: shard r already at slot r of its own output
+    bufs = [torch.zeros(n * sc, dtype=torch.int32, device="cuda") for _ in range(n)]
+    for r in range(n):
+        bufs[r][r * sc:(r + 1) * sc] = ins[r]
+    rra.rra_all_gather([bufs[r][r * sc:(r + 1) * sc] for r in range(n)], bufs, sc, rra.RRA_INT32,
+                       rra.RRA_ALGO_COPY_ENGINE)
+    _status_ok()
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(bufs[r], "int32"), want[r], "copy engine in place r=%d" % r)
+
+
+@pytest.mark.parametrize("max_ctas", [1, 8, 19, 64])
+def test_sm_budget_keeps_results(max_ctas):
+    n, count = 8, 1_000_003
+    xs = inputs.make_ranks(n, count, "float32", "normal", seed=max_ctas)
+    rra.rra_set_max_ctas(max_ctas)
+    try:
+        for algo in AR:
+            got = run_allreduce(xs, "float32", algo)
+            want, _, _ = oracle.allreduce(algo, xs, "float32")
+            for r in (0, n - 1):
+                _check(got[r], want[r], "float32", "%s max_ctas=%d" % (algo, max_ctas))
+        text = rra.rra_dump_recent().strip().splitlines()[-1]
+        assert "algo=two_shot" in text or "algo=ring" in text or "algo=one_shot" in text
+    finally:
+        rra.rra_set_max_ctas(0)
 
 
 @pytest.mark.parametrize("algo", list(RSAG))
@@ -307,3 +365,44 @@ def test_cuda_graph_capture():
         _status_ok()
         for r in range(n):
             g.assert_bits_equal(g.to_host(outs[r], "float32"), want[r], "graph replay %d" % rep)
+
+
+@pytest.mark.parametrize("dtype", ["bfloat16", "float32"])
+@pytest.mark.parametrize("tokens", inputs.TP_TOKENS)
+@pytest.mark.parametrize("n", [2, 8])
+def test_allreduce_rmsnorm(dtype, tokens, n):
+    # fused all-reduce + RMSNorm on [tokens, 5120]: within the 1e-2 relative
+    # bar of the oracle (float64 normalisation of the float32 sums)
+    g = G()
+    hidden = inputs.TP_HIDDEN
+    xs = inputs.make_ranks(n, tokens * hidden, dtype, "normal", seed=tokens + n)
+    gamma = inputs.make_ranks(1, hidden, dtype, "normal", seed=99)[0]
+    ins = [g.to_dev(x, dtype) for x in xs]
+    outs = g.empty(n, tokens * hidden, dtype)
+    rra.rra_allreduce_rmsnorm(ins, outs, g.to_dev(gamma, dtype), hidden, eps=1e-6)
+    _status_ok()
+    want = oracle.allreduce_rmsnorm(xs, gamma, 1e-6, dtype, hidden)
+    for r in range(n):
+        got = g.to_host(outs[r], dtype)
+        if dtype == "bfloat16":
+            assert g.bf16_rel_ok(got, want[r]), r
+        else:
+            w = want[r].astype(np.float64)
+            assert np.all(np.abs(got.astype(np.float64) - w) <= 1e-5 * np.abs(w) + 1e-6), r
+        assert got.tobytes() == g.to_host(outs[0], dtype).tobytes()
+
+
+@pytest.mark.parametrize("hidden", [1, 7, 100, 4096, 12345])
+def test_allreduce_rmsnorm_odd_rows_and_in_place(hidden):
+    g = G()
+    n, rows = 3, 5
+    xs = inputs.make_ranks(n, rows * hidden, "float32", "normal", seed=hidden)
+    gamma = inputs.make_ranks(1, hidden, "float32", "normal", seed=1)[0]
+    ins = [g.to_dev(x, "float32") for x in xs]
+    rra.rra_allreduce_rmsnorm(ins, ins, g.to_dev(gamma, "float32"), hidden, eps=1e-5)
+    _status_ok()
+    want = oracle.allreduce_rmsnorm(xs, gamma, 1e-5, "float32", hidden)
+    for r in range(n):
+        got = g.to_host(ins[r], "float32").astype(np.float64)
+        w = want[r].astype(np.float64)
+        assert np.all(np.abs(got - w) <= 1e-5 * np.abs(w) + 1e-6)
