@@ -86,6 +86,7 @@ def _declare(lib):
         "rra_init": (i, [i, sz]),
         "rra_finalize": (i, [i]),
         "rra_allreduce": (i, [vpp, vpp, i, sz, i, i, i, vp]),
+        "rra_allreduce_two_shot_static": (i, [vpp, vpp, i, sz, i, i, vp]),
         "rra_reduce_scatter": (i, [vpp, vpp, i, sz, i, i, i, vp]),
         "rra_all_gather": (i, [vpp, vpp, i, sz, i, i, vp]),
         "rra_allreduce_rmsnorm": (i, [vpp, vpp, i, sz, sz, vp, ctypes.c_float, i, vp]),
@@ -201,6 +202,18 @@ def rra_allreduce(bufs, outs, count=None, dtype=None, op=RRA_SUM, algo=RRA_ALGO_
     st = load().rra_allreduce(_ptr_array(bufs), _ptr_array(outs), n, count, dtype, op, algo,
                               _stream(stream, bufs[0] if bufs else None))
     return _ret(st, "rra_allreduce", check)
+
+
+def rra_allreduce_two_shot_static(bufs, outs, count=None, dtype=None, op=RRA_SUM, stream=None,
+                                  check=True, nranks=None) -> int:
+    """Two-shot all-reduce whose scratch is a static device array inside the
+    library: no rra_init and no device allocation, for callers that may not
+    allocate.  Calls that overlap on the GPU share that array and race."""
+    count, dtype = _resolve(bufs, count, dtype)
+    n = len(bufs) if nranks is None else nranks
+    st = load().rra_allreduce_two_shot_static(_ptr_array(bufs), _ptr_array(outs), n, count, dtype, op,
+                                              _stream(stream, bufs[0] if bufs else None))
+    return _ret(st, "rra_allreduce_two_shot_static", check)
 
 
 def rra_reduce_scatter(bufs, outs, recvcount=None, dtype=None, op=RRA_SUM, algo=RRA_ALGO_AUTO,

@@ -130,6 +130,39 @@ rra_status_t rra_finalize(int device);
 rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nranks, size_t count,
                            rra_dtype_t dtype, rra_op_t op, rra_algo_t algo, rra_stream_t stream);
 
+/** Two-shot all-reduce that allocates nothing.  The pages have no
+ *  counterpart: this exists for callers that may not allocate device
+ *  memory, and so cannot call rra_init (which calls cudaMalloc for its
+ *  workspace).  Examples: a plugin inside a framework whose allocator owns
+ *  all device memory, or code under a memory budget that forbids new
+ *  allocations after start-up.
+ *  - Same arguments, result and summation order as rra_allreduce with
+ *    RRA_ALGO_TWO_SHOT (outs[r][i] = SUM_k bufs[k][i], chunk r reduced in
+ *    ascending rank order, then gathered back).  The caller passes the
+ *    inputs and outputs; in place is allowed as there.
+ *  - Scratch: the kernel's status block, call epoch and step flags live in
+ *    a static device array of 16,640 bytes inside librra.so, which every
+ *    GPU that loads the library holds until the process exits.  It holds
+ *    flags for at most 8 ranks x 16 channels; more than 8 ranks is
+ *    RRA_ERR_UNSUPPORTED.  Messages of any size are split over at most 16
+ *    channels per rank.
+ *  - No cudaMalloc, cudaFree or allocating library routine is called.
+ *    The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first
+ *    call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last
+ *    call's contents (the status block is cleared at the start of each
+ *    call; the flags carry a per-call epoch and need no clearing).  Calls
+ *    that overlap on the GPU -- on two streams without ordering, or
+ *    together with another copy of this call -- race on it.
+ *  - Device waits are bounded (500 ms); a wait that expires ends the
+ *    kernel early, and this entry point offers no status query for it.
+ *  Errors: RRA_ERR_INVALID_ARG, RRA_ERR_UNSUPPORTED, RRA_ERR_ALIAS,
+ *  RRA_ERR_CUDA.  count == 0 returns RRA_SUCCESS without a launch. */
+rra_status_t rra_allreduce_two_shot_static(const void* const* bufs, void* const* outs, int nranks,
+                                           size_t count, rra_dtype_t dtype, rra_op_t op,
+                                           rra_stream_t stream);
+
 /** Reduce-scatter ([ILP] "Direct answer": sum across ranks, each keeps only
  *  its slice).  bufs[r] holds nranks*recvcount elements; outs[r]
  *  (recvcount elements) receives slice r of the sum:
