@@ -1,12 +1,14 @@
 // kernels_ring.cu -- ring all-reduce and its reduce-scatter / all-gather
-// halves.
+// halves, with the Simple or the LL protocol on the ring's links.
 //
 // "NCCL collectives, ring all-reduce & launching TP/PP", sections "Direct
 // answer" and "Deep dive": ring all-reduce = reduce-scatter + all-gather;
 // the ring pipelines the data in N chunks so every link is busy.
 // "Collective communication: NCCL's algorithms and protocols...", section
 // "Algorithms": n-1 reduce-scatter steps and n-1 all-gather steps, each
-// GPU sending and receiving 2(n-1)/n S.
+// GPU sending and receiving 2(n-1)/n S; section "Protocols": LL lines carry
+// 4 data bytes and a 4-byte flag that the receiver polls, Simple writes a
+// block, fences and then raises a flag.
 //
 // Schedule, per rank r (indices mod n):
 //   RS step s = 0..n-2: send the partial of chunk (r-s-1) to r+1; the
@@ -16,28 +18,46 @@
 //
 // Design on one GPU: one persistent cooperative launch of n x C CTAs; CTA
 // (r, ch) is channel ch of virtual rank r and every one of its 16 warps is
-// an independent pipeline.  The link r -> r+1 of (channel, warp) is a
-// FIFO of K slots in the workspace, small enough to stay in L2, with a head
-// counter (messages posted by the sender) and a tail counter (messages
-// consumed by the receiver).  Send = write the slot, __syncwarp, release
-// the head (data -> fence -> flag: the Simple protocol of the page's
-// "Protocols" section); receive = acquire the head, read the slot, release
-// the tail.  Each step moves G slices of the channel's part of a chunk;
-// the receiver of slice g in step s+1 needs slice g of step s, posted G
-// messages earlier, so the flag latency hides behind the other slices.
-// bfloat16 partial sums travel as float32 and are rounded once, at the
-// final reduce-scatter step.  Only the inputs are read from HBM and only
-// the outputs written to it; the slots stay in L2.
+// an independent pipeline.  The link r -> r+1 of (channel, warp) is a FIFO
+// of K slots in the workspace, small enough to stay in L2.  Each step moves
+// G messages (slices); the receiver of slice g in step s+1 needs slice g of
+// step s, posted G messages earlier, so latency hides behind the other
+// slices.  A sender waits for a free slot on the tail counter the receiver
+// raises (credits).
+//   Simple: write the slot, __syncwarp, fence, raise the head counter; the
+//     receiver acquires the head counter before reading the slot.
+//   LL: every 4-byte word travels in an 8-byte line with a flag, written
+//     and read as one 64-bit access (single-copy atomic), so no fence and
+//     no head counter are needed: the receiver polls the lines themselves.
+//     The flag is the call tag doubled plus the slot's reuse parity, so a
+//     line left from the slot's previous use or an earlier call never
+//     matches.  Credits are raised once per G messages.
+// The rank's own input for the next message is loaded before its wait, so
+// the HBM latency overlaps the wait.  bfloat16 partial sums travel as
+// float32 and are rounded once, at the final reduce-scatter step.  Only the
+// inputs are read from HBM and only the outputs written to it.
 #include "common.cuh"
 
 namespace rra {
 
-template <int DT, bool VEC>
+__device__ __forceinline__ void st_ll_pair(void* p, uint32_t flag, uint32_t a, uint32_t b) {
+  const unsigned long long x = ((unsigned long long)flag << 32) | a;
+  const unsigned long long y = ((unsigned long long)flag << 32) | b;
+  asm volatile("st.volatile.global.v2.u64 [%0], {%1,%2};" ::"l"(p), "l"(x), "l"(y) : "memory");
+}
+
+__device__ __forceinline__ void ld_ll_pair(const void* p, unsigned long long& x, unsigned long long& y) {
+  asm volatile("ld.volatile.global.v2.u64 {%0,%1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+}
+
+template <int DT, bool VEC, int PROTO>
 struct RingWarp {
   static constexpr int PU = Elem<DT>::kPerUnit;
   static constexpr int ES = Elem<DT>::kSize;
   static constexpr int AW = Elem<DT>::kAccWords;
   static constexpr int UPT = kRingUnitsPerThread;
+  // bytes a slot reserves per unit (per accumulator word: 16 B Simple, 32 B LL)
+  static constexpr int WB = PROTO == kProtoLL ? 32 : 16;
 
   const RingArgs& a;
   int r, prev, next, lane;
@@ -46,7 +66,7 @@ struct RingWarp {
   uint64_t *head_in, *tail_in, *head_out, *tail_out;
   char *fifo_in, *fifo_out;
   uint32_t m_in = 0, m_out = 0;
-  uint64_t seen_head = 0, seen_tail = 0;  // lane 0: last values observed
+  uint64_t seen_head = 0, seen_tail = 0;  // last values observed by the polling lanes
 
   __device__ RingWarp(const RingArgs& args, int r_, int ch, int warp, int lane_, int W, uint64_t E_,
                       uint32_t tag_)
@@ -60,26 +80,29 @@ struct RingWarp {
     tail_in = a.tail + link_in * W + warp;
     head_out = a.head + link_out * W + warp;
     tail_out = a.tail + link_out * W + warp;
-    const size_t wregion = (size_t)warp * 32 * UPT * 16 * AW;
+    const size_t wregion = (size_t)warp * 32 * UPT * AW * WB;
     fifo_in = a.fifo + link_in * a.K * a.slot_bytes + wregion;
     fifo_out = a.fifo + link_out * a.K * a.slot_bytes + wregion;
   }
 
-  // Lane 0 waits for the next incoming message and / or a free outgoing
-  // slot; the warp learns the outcome.  False: the call was aborted.
+  __device__ __forceinline__ uint32_t ll_flag(uint32_t m) const {
+    return (tag << 1) + ((m / (uint32_t)a.K) & 1u) + 1u;
+  }
+
+  // Wait for the next incoming message (Simple: lane 0 acquires the head
+  // counter) and / or a free outgoing slot (lane 1 acquires the tail
+  // counter); the two waits run side by side.  False: the call aborted.
   __device__ __forceinline__ bool wait(bool need_in, bool need_out, int step) {
     int ok = 1;
-    if (lane == 0) {
-      if (need_in) {
-        const uint64_t want = E | (uint64_t)(m_in + 1);
-        if (seen_head < want) ok = wait_geq(head_in, want, &seen_head, a.wait, tag, r, prev, step);
-      }
-      if (ok && need_out && m_out >= (uint32_t)a.K) {
-        const uint64_t want = E | (uint64_t)(m_out - a.K + 1);
-        if (seen_tail < want) ok = wait_geq(tail_out, want, &seen_tail, a.wait, tag, r, next, step);
-      }
+    if (PROTO == kProtoSimple && need_in && lane == 0) {
+      const uint64_t want = E | (uint64_t)(m_in + 1);
+      if (seen_head < want) ok = wait_geq(head_in, want, &seen_head, a.wait, tag, r, prev, step);
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (need_out && lane == 1 && m_out >= (uint32_t)a.K) {
+      const uint64_t want = E | (uint64_t)(m_out - a.K + 1);
+      if (seen_tail < want) ok = wait_geq(tail_out, want, &seen_tail, a.wait, tag, r, next, step);
+    }
+    ok = __all_sync(0xffffffffu, ok);
     __syncwarp();
     return ok != 0;
   }
@@ -87,10 +110,17 @@ struct RingWarp {
   // Publish the message just written and / or free the slot just read.
   __device__ __forceinline__ void post(bool sent, bool consumed) {
     __syncwarp();
-    if (lane == 0) {
-      fence_acq_rel();
-      if (sent) st_relaxed(head_out, E | (uint64_t)(m_out + 1));
-      if (consumed) st_relaxed(tail_in, E | (uint64_t)(m_in + 1));
+    if (PROTO == kProtoSimple) {
+      if (lane == 0) {
+        fence_acq_rel();
+        if (sent) st_relaxed(head_out, E | (uint64_t)(m_out + 1));
+        if (consumed) st_relaxed(tail_in, E | (uint64_t)(m_in + 1));
+      }
+    } else if (lane == 0) {
+      if (consumed && ((m_in + 1) % (uint32_t)a.G) == 0) st_release(tail_in, E | (uint64_t)(m_in + 1));
+      // progress marker only (the lines carry their own flags): lets a peer
+      // that gives up tell a rank that never sent from one stuck behind it
+      if (sent && ((m_out + 1) % (uint32_t)a.G) == 0) st_relaxed(head_out, E | (uint64_t)(m_out + 1));
     }
     if (sent) ++m_out;
     if (consumed) ++m_in;
@@ -103,39 +133,110 @@ struct RingWarp {
     return fifo_out + (size_t)(m_out % (uint32_t)a.K) * a.slot_bytes;
   }
 
-  // Reduce-scatter send of chunk c (first step: own data; later steps:
-  // received partial (+) own data).
-  __device__ __forceinline__ bool rs_step(int c, bool first, size_t base, int step) {
-    if (!wait(!first, true, step)) return false;
+  // unit j of this lane, word q, in a slot
+  __device__ __forceinline__ size_t word_off(int j, int q) const {
+    return ((size_t)(j * 32 + lane) * AW + q) * WB;
+  }
+
+  __device__ __forceinline__ void put(char* slot, int j, int q, uint4 w) const {
+    char* p = slot + word_off(j, q);
+    if (PROTO == kProtoSimple) {
+      st_l2(p, w);
+    } else {
+      const uint32_t f = ll_flag(m_out);
+      st_ll_pair(p, f, w.x, w.y);
+      st_ll_pair(p + 16, f, w.z, w.w);
+    }
+  }
+
+  // Read the `nw` words of each valid unit of the incoming message.  LL:
+  // poll every line until its flag matches (bounded); false on abort.
+  __device__ __forceinline__ bool get(const char* slot, const int* v, int nw, uint4 (*w)[2], int step) {
+    if (PROTO == kProtoSimple) {
+#pragma unroll
+      for (int j = 0; j < UPT; ++j)
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (q < nw && v[j] > 0) w[j][q] = ld_l2(slot + word_off(j, q));
+      return true;
+    }
+    const uint32_t f = ll_flag(m_in);
+    bool done = false;
+    uint64_t t0 = 0;
+    int ok = 1;
+    for (uint32_t it = 0;; ++it) {
+      if (!done) {
+        bool all = true;
+#pragma unroll
+        for (int j = 0; j < UPT; ++j)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            if (q >= nw || v[j] == 0) continue;
+            unsigned long long l0, l1, l2, l3;
+            const char* p = slot + word_off(j, q);
+            ld_ll_pair(p, l0, l1);
+            ld_ll_pair(p + 16, l2, l3);
+            all = all && (uint32_t)(l0 >> 32) == f && (uint32_t)(l1 >> 32) == f &&
+                  (uint32_t)(l2 >> 32) == f && (uint32_t)(l3 >> 32) == f;
+            w[j][q] = make_uint4((uint32_t)l0, (uint32_t)l1, (uint32_t)l2, (uint32_t)l3);
+          }
+        done = all;
+      }
+      if (__all_sync(0xffffffffu, done)) break;
+      if (it == 0) t0 = globaltimer();
+      int give_up = 0;
+      if ((it & 15u) == 15u && lane == 0) {
+        if (aborted(a.wait.status, tag)) {
+          give_up = 1;
+        } else if (globaltimer() - t0 > a.wait.timeout_ns || it >= kMaxSpin) {
+          const bool root = (ld_acquire(head_in) >> 32) != (E >> 32);  // prev sent nothing
+          record_error(a.wait.status, RRA_ERR_TIMEOUT, r, prev, step, tag, root);
+          give_up = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, give_up, 0)) {
+        ok = 0;
+        break;
+      }
+      if (!done) __nanosleep(32);
+    }
+    return ok != 0;
+  }
+
+  __device__ __forceinline__ void load_x(int c, size_t base, uint4* xv, int* v) const {
     const char* x = static_cast<const char*>(a.in[r]) + a.ibase[c] * ES;
-    char* si = slot_in();
-    char* so = slot_out();
-    uint4 xv[UPT];
-    int v[UPT];
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
       const size_t u = base + (size_t)j * 32 + lane;
       v[j] = unit_valid<DT>(u, a.len[c]);
       if (v[j] > 0) xv[j] = load_in<DT, VEC>(x, u, v[j]);
     }
+  }
+
+  // Reduce-scatter send of chunk c (first step: own data; later steps:
+  // received partial (+) own data).
+  __device__ __forceinline__ bool rs_step(int c, bool first, size_t base, int step) {
+    uint4 xv[UPT];
+    int v[UPT];
+    load_x(c, base, xv, v);
+    if (!wait(!first, true, step)) return false;
+    uint4 p[UPT][2];
+    if (!first && !get(slot_in(), v, AW, p, step)) return false;
+    char* so = slot_out();
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
       if (v[j] == 0) continue;
-      const size_t w = (size_t)(j * 32 + lane) * AW;
       Acc s;
       if (first) {
         acc_init<DT>(s, xv[j]);
       } else {
-        uint4 p[AW];
-#pragma unroll
-        for (int q = 0; q < AW; ++q) p[q] = ld_l2(si + (w + q) * 16);
-        acc_from_words<DT>(s, p);
+        acc_from_words<DT>(s, p[j]);
         acc_add<DT>(s, xv[j]);
       }
-      uint4 o[AW];
+      uint4 o[2];
       acc_to_words<DT>(s, o);
 #pragma unroll
-      for (int q = 0; q < AW; ++q) st_l2(so + (w + q) * 16, o[q]);
+      for (int q = 0; q < AW; ++q) put(so, j, q, o[q]);
     }
     post(true, !first);
     return true;
@@ -144,36 +245,28 @@ struct RingWarp {
   // Last reduce-scatter step: chunk r is complete; store it, and forward it
   // (as the first all-gather message) when `fwd`.
   __device__ __forceinline__ bool rs_final(size_t base, bool fwd, int step) {
-    if (!wait(a.n > 1, fwd, step)) return false;
-    const char* x = static_cast<const char*>(a.in[r]) + a.ibase[r] * ES;
-    char* y = static_cast<char*>(a.out[r]) + a.obase[r] * ES;
-    char* si = slot_in();
-    char* so = slot_out();
     uint4 xv[UPT];
     int v[UPT];
-#pragma unroll
-    for (int j = 0; j < UPT; ++j) {
-      const size_t u = base + (size_t)j * 32 + lane;
-      v[j] = unit_valid<DT>(u, a.len[r]);
-      if (v[j] > 0) xv[j] = load_in<DT, VEC>(x, u, v[j]);
-    }
+    load_x(r, base, xv, v);
+    if (!wait(a.n > 1, fwd, step)) return false;
+    uint4 p[UPT][2];
+    if (a.n > 1 && !get(slot_in(), v, AW, p, step)) return false;
+    char* y = static_cast<char*>(a.out[r]) + a.obase[r] * ES;
+    char* so = slot_out();
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
       if (v[j] == 0) continue;
       const size_t u = base + (size_t)j * 32 + lane;
       Acc s;
       if (a.n > 1) {
-        uint4 p[AW];
-#pragma unroll
-        for (int q = 0; q < AW; ++q) p[q] = ld_l2(si + ((size_t)(j * 32 + lane) * AW + q) * 16);
-        acc_from_words<DT>(s, p);
+        acc_from_words<DT>(s, p[j]);
         acc_add<DT>(s, xv[j]);
       } else {
         acc_init<DT>(s, xv[j]);
       }
       const uint4 out = acc_narrow<DT>(s);
       store_out<DT, VEC, true>(y, u, v[j], out);
-      if (fwd) st_l2(so + (size_t)(j * 32 + lane) * 16, out);
+      if (fwd) put(so, j, 0, out);
     }
     post(fwd, a.n > 1);
     return true;
@@ -181,24 +274,18 @@ struct RingWarp {
 
   // All-gather start (all-gather mode): the own shard is chunk r.
   __device__ __forceinline__ bool ag_first(size_t base, int step) {
-    if (!wait(false, true, step)) return false;
-    const char* x = static_cast<const char*>(a.in[r]) + a.ibase[r] * ES;
-    char* y = static_cast<char*>(a.out[r]) + a.obase[r] * ES;
-    char* so = slot_out();
     uint4 xv[UPT];
     int v[UPT];
-#pragma unroll
-    for (int j = 0; j < UPT; ++j) {
-      const size_t u = base + (size_t)j * 32 + lane;
-      v[j] = unit_valid<DT>(u, a.len[r]);
-      if (v[j] > 0) xv[j] = load_in<DT, VEC>(x, u, v[j]);
-    }
+    load_x(r, base, xv, v);
+    if (!wait(false, true, step)) return false;
+    char* y = static_cast<char*>(a.out[r]) + a.obase[r] * ES;
+    char* so = slot_out();
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
       if (v[j] == 0) continue;
       const size_t u = base + (size_t)j * 32 + lane;
       store_out<DT, VEC, true>(y, u, v[j], xv[j]);
-      st_l2(so + (size_t)(j * 32 + lane) * 16, xv[j]);
+      put(so, j, 0, xv[j]);
     }
     post(true, false);
     return true;
@@ -206,24 +293,20 @@ struct RingWarp {
 
   // All-gather step: receive chunk c, store it, forward it unless `last`.
   __device__ __forceinline__ bool ag_step(int c, bool last, size_t base, int step) {
-    if (!wait(true, !last, step)) return false;
-    char* y = static_cast<char*>(a.out[r]) + a.obase[c] * ES;
-    char* si = slot_in();
-    char* so = slot_out();
-    uint4 yv[UPT];
     int v[UPT];
 #pragma unroll
-    for (int j = 0; j < UPT; ++j) {
-      const size_t u = base + (size_t)j * 32 + lane;
-      v[j] = unit_valid<DT>(u, a.len[c]);
-      if (v[j] > 0) yv[j] = ld_l2(si + (size_t)(j * 32 + lane) * 16);
-    }
+    for (int j = 0; j < UPT; ++j) v[j] = unit_valid<DT>(base + (size_t)j * 32 + lane, a.len[c]);
+    if (!wait(true, !last, step)) return false;
+    uint4 p[UPT][2];
+    if (!get(slot_in(), v, 1, p, step)) return false;
+    char* y = static_cast<char*>(a.out[r]) + a.obase[c] * ES;
+    char* so = slot_out();
 #pragma unroll
     for (int j = 0; j < UPT; ++j) {
       if (v[j] == 0) continue;
       const size_t u = base + (size_t)j * 32 + lane;
-      store_out<DT, VEC, true>(y, u, v[j], yv[j]);
-      if (!last) st_l2(so + (size_t)(j * 32 + lane) * 16, yv[j]);
+      store_out<DT, VEC, true>(y, u, v[j], p[j][0]);
+      if (!last) put(so, j, 0, p[j][0]);
     }
     post(!last, true);
     return true;
@@ -270,8 +353,8 @@ struct RingWarp {
   }
 };
 
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kRingThreads) ring_kernel(const __grid_constant__ RingArgs a) {
+template <int DT, bool VEC, int PROTO>
+__global__ void __launch_bounds__(kRingThreads, 1) ring_kernel(const __grid_constant__ RingArgs a) {
   __shared__ uint32_t s_epoch;
   if (threadIdx.x == 0) s_epoch = read_epoch(a.wait.sync);
   __syncthreads();
@@ -279,32 +362,33 @@ __global__ void __launch_bounds__(kRingThreads) ring_kernel(const __grid_constan
   const int r = blockIdx.x % a.n, ch = blockIdx.x / a.n;
   const int W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (r != a.wait.skip_rank) {
-    RingWarp<DT, VEC> w(a, r, ch, warp, lane, W, (uint64_t)epoch << 32, epoch + 1u);
+    RingWarp<DT, VEC, PROTO> w(a, r, ch, warp, lane, W, (uint64_t)epoch << 32, epoch + 1u);
     w.run(ch, warp);
   }
   arrive_end(a.wait.sync, epoch);
 }
 
 template <int DT, bool VEC>
-static const void* ring_fn() {
-  return reinterpret_cast<const void*>(&ring_kernel<DT, VEC>);
+static const void* ring_fn(int proto) {
+  return proto == kProtoLL ? reinterpret_cast<const void*>(&ring_kernel<DT, VEC, kProtoLL>)
+                           : reinterpret_cast<const void*>(&ring_kernel<DT, VEC, kProtoSimple>);
 }
 
-static const void* ring_pick(int dt, bool vec) {
-  if (dt == RRA_INT32) return vec ? ring_fn<RRA_INT32, true>() : ring_fn<RRA_INT32, false>();
-  if (dt == RRA_FLOAT32) return vec ? ring_fn<RRA_FLOAT32, true>() : ring_fn<RRA_FLOAT32, false>();
-  if (dt == RRA_BFLOAT16) return vec ? ring_fn<RRA_BFLOAT16, true>() : ring_fn<RRA_BFLOAT16, false>();
+static const void* ring_pick(int dt, bool vec, int proto) {
+  if (dt == RRA_INT32) return vec ? ring_fn<RRA_INT32, true>(proto) : ring_fn<RRA_INT32, false>(proto);
+  if (dt == RRA_FLOAT32) return vec ? ring_fn<RRA_FLOAT32, true>(proto) : ring_fn<RRA_FLOAT32, false>(proto);
+  if (dt == RRA_BFLOAT16) return vec ? ring_fn<RRA_BFLOAT16, true>(proto) : ring_fn<RRA_BFLOAT16, false>(proto);
   return nullptr;
 }
 
-cudaError_t ring_occupancy(int dt, bool vec, int* max_blocks_per_sm) {
-  const void* f = ring_pick(dt, vec);
+cudaError_t ring_occupancy(int dt, bool vec, int proto, int* max_blocks_per_sm) {
+  const void* f = ring_pick(dt, vec, proto);
   if (!f) return cudaErrorInvalidValue;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(max_blocks_per_sm, f, kRingThreads, 0);
 }
 
-cudaError_t launch_ring(int dt, bool vec, const RingArgs& a, int grid, cudaStream_t s) {
-  const void* f = ring_pick(dt, vec);
+cudaError_t launch_ring(int dt, bool vec, int proto, const RingArgs& a, int grid, cudaStream_t s) {
+  const void* f = ring_pick(dt, vec, proto);
   if (!f) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -32,11 +32,8 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
   const int C = a.channels;
   const size_t tile = (size_t)a.tile_units;
   const size_t wofs = (size_t)warp * 32 * UPT;
-  size_t units[N];
-#pragma unroll
-  for (int c = 0; c < N; ++c) units[c] = (a.chunk_len[c] + PU - 1) / PU;
   const size_t per_iter = (size_t)C * tile;
-  const size_t iters = (units[0] + per_iter - 1) / per_iter;  // chunk 0 is the longest
+  const size_t iters = ((a.chunk_len[0] + PU - 1) / PU + per_iter - 1) / per_iter;  // chunk 0 is the longest
   uint64_t* my_flag = a.progress + ((size_t)r * C + ch) * W + warp;
 
   for (size_t it = 0; it < iters; ++it) {
@@ -72,42 +69,52 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
     __syncwarp();
     if (lane == 0) st_release(my_flag, E | (uint64_t)(it + 1));
 
-    // phase 2: all-gather part
-    for (int j = 1; j < N; ++j) {
-      const int q = (r + j) % N;
-      if (t0 >= units[q]) continue;
+    // phase 2: all-gather part.  Lane j waits for peer (r + j) mod N, so the
+    // n-1 acquires run side by side; __syncwarp then orders every lane's
+    // reads after all of them, and the n-1 tiles are read with all loads in
+    // flight at once.
+    {
       int ok = 1;
-      if (lane == 0) {
-        uint64_t seen;
-        ok = wait_geq(a.progress + ((size_t)q * C + ch) * W + warp, E | (uint64_t)(it + 1), &seen,
-                      a.wait, tag, r, q, (int)it);
+      if (lane >= 1 && lane < N) {
+        const int q = (r + lane) % N;
+        if (t0 < (a.chunk_len[q] + PU - 1) / PU) {
+          uint64_t seen;
+          ok = wait_geq(a.progress + ((size_t)q * C + ch) * W + warp, E | (uint64_t)(it + 1), &seen,
+                        a.wait, tag, r, q, (int)it);
+        }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ok = __all_sync(0xffffffffu, ok);
       __syncwarp();
       if (!ok) return;
-      const size_t lo = a.chunk_lo[q] * ES;
-      const size_t len = a.chunk_len[q];
-      const char* src = static_cast<const char*>(a.out[q]) + lo;
-      char* dst = static_cast<char*>(a.out[r]) + lo;
-      uint4 y[UPT];
-      int v[UPT];
+    }
+    uint4 y[N > 1 ? N - 1 : 1][UPT];
+    int v[N > 1 ? N - 1 : 1][UPT];
+#pragma unroll
+    for (int j = 1; j < N; ++j) {
+      const int q = (r + j) % N;
+      const char* src = static_cast<const char*>(a.out[q]) + a.chunk_lo[q] * ES;
 #pragma unroll
       for (int jj = 0; jj < UPT; ++jj) {
         const size_t u = t0 + (size_t)jj * 32 + lane;
-        v[jj] = unit_valid<DT>(u, len);
-        if (v[jj] > 0) y[jj] = load_shared_out<DT, VEC>(src, u, v[jj]);
+        v[j - 1][jj] = unit_valid<DT>(u, a.chunk_len[q]);
+        if (v[j - 1][jj] > 0) y[j - 1][jj] = load_shared_out<DT, VEC>(src, u, v[j - 1][jj]);
       }
+    }
+#pragma unroll
+    for (int j = 1; j < N; ++j) {
+      const int q = (r + j) % N;
+      char* dst = static_cast<char*>(a.out[r]) + a.chunk_lo[q] * ES;
 #pragma unroll
       for (int jj = 0; jj < UPT; ++jj) {
         const size_t u = t0 + (size_t)jj * 32 + lane;
-        if (v[jj] > 0) store_out<DT, VEC, true>(dst, u, v[jj], y[jj]);
+        if (v[j - 1][jj] > 0) store_out<DT, VEC, true>(dst, u, v[j - 1][jj], y[j - 1][jj]);
       }
     }
   }
 }
 
 template <int N, int DT, bool VEC>
-__global__ void __launch_bounds__(kDirectThreads) twoshot_kernel(const __grid_constant__ TwoShotArgs a) {
+__global__ void __launch_bounds__(kDirectThreads, 1) twoshot_kernel(const __grid_constant__ TwoShotArgs a) {
   __shared__ uint32_t s_epoch;
   if (threadIdx.x == 0) s_epoch = read_epoch(a.wait.sync);
   __syncthreads();

@@ -241,6 +241,16 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
   return cuda_status(launch_twoshot(n, dt, vec, a, n * (int)c, st));
 }
 
+// The ring's link protocol: RRA_RING_PROTO=simple|ll forces one; otherwise
+// LL up to the measured crossover (bytes per chunk), Simple above.
+int ring_proto(size_t chunk_bytes) {
+  const char* p = std::getenv("RRA_RING_PROTO");
+  if (p && !std::strcmp(p, "simple")) return kProtoSimple;
+  if (p && !std::strcmp(p, "ll")) return kProtoLL;
+  static const long limit = env_long("RRA_RING_LL_MAX_BYTES", -1);
+  return (limit < 0 || (long)chunk_bytes <= limit) ? kProtoLL : kProtoSimple;
+}
+
 // mode: kRingAllReduce / kRingReduceScatter / kRingAllGather.  ibase, obase,
 // len: per chunk, in elements.
 rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int n, int mode,
@@ -260,16 +270,20 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   a.n = n;
   a.mode = mode;
   a.slice_units = kRingThreads * kRingUnitsPerThread;
-  // K > G: with K == G every rank could fill its outgoing FIFO in the first
-  // step and then wait for a credit its successor can only give after
-  // sending too (sends minus receives of a rank never exceed G, so n full
-  // FIFOs of K > G slots cannot all be pending at once).
+  const int proto = ring_proto(maxu * 16);
+  // Credits: a rank's sends minus receives never exceed G.  Simple raises a
+  // credit per message, so K > G keeps n full FIFOs from all being pending
+  // at once (with K == G every rank could fill its FIFO in the first step
+  // and wait for a credit its successor gives only after sending too).  LL
+  // raises one credit per G messages, which lags by up to G-1 more, so it
+  // needs K >= 2G.
   a.G = (int)std::max(1L, env_long("RRA_RING_G", 4));
-  a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", 2L * a.G));
+  const long kmin = proto == kProtoLL ? 2L * a.G : (long)a.G + 1;
+  a.K = (int)std::max(kmin, env_long("RRA_RING_K", 2L * a.G));
   const int aw = dt == RRA_BFLOAT16 ? 2 : 1;
-  a.slot_bytes = (size_t)a.slice_units * 16 * aw;
+  a.slot_bytes = (size_t)a.slice_units * aw * (proto == kProtoLL ? 32 : 16);
   int occ = 0;
-  cudaError_t err = ring_occupancy(dt, vec, &occ);
+  cudaError_t err = ring_occupancy(dt, vec, proto, &occ);
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   const size_t need = (maxu + (size_t)a.G * a.slice_units - 1) / ((size_t)a.G * a.slice_units);
   const size_t fifo_cap = s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes);
@@ -282,7 +296,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   a.tail = s->ws.flags + kLinkFlags;
   a.wait = wait_cfg(s);
   *grid_out = n * (int)c;
-  return cuda_status(launch_ring(dt, vec, a, n * (int)c, st));
+  return cuda_status(launch_ring(dt, vec, proto, a, n * (int)c, st));
 }
 
 bool all_aligned16(const void* const* p, int n) {

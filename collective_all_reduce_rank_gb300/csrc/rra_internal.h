@@ -90,8 +90,10 @@ struct TwoShotArgs {
   WaitCfg wait;
 };
 
-// Ring (persistent, cooperative): all-reduce, reduce-scatter or all-gather.
+// Ring (persistent, cooperative): all-reduce, reduce-scatter or all-gather,
+// with the Simple or the LL protocol on its links.
 enum RingMode : int { kRingAllReduce = 0, kRingReduceScatter = 1, kRingAllGather = 2 };
+enum RingProto : int { kProtoSimple = 0, kProtoLL = 1 };
 
 struct RingArgs {
   const void* in[kMaxRanks];
@@ -130,7 +132,7 @@ struct LLArgs {
 constexpr int kDirectThreads = 512;
 constexpr int kRingThreads = 512;
 constexpr int kRingUnitsPerThread = 2;
-constexpr int kTwoShotUnitsPerThread = 2;
+constexpr int kTwoShotUnitsPerThread = 1;
 constexpr int kLLThreads = 256;
 
 // SM budget set by rra_set_max_ctas (0: none); kernels_direct.cu caps its
@@ -161,8 +163,8 @@ cudaError_t launch_allreduce_rmsnorm(int n, int dt, bool vec, const void* const*
 // the launch fails.  *max_blocks_per_sm reports the occupancy limit.
 cudaError_t twoshot_occupancy(int n, int dt, bool vec, int* max_blocks_per_sm);
 cudaError_t launch_twoshot(int n, int dt, bool vec, const TwoShotArgs& a, int grid, cudaStream_t s);
-cudaError_t ring_occupancy(int dt, bool vec, int* max_blocks_per_sm);
-cudaError_t launch_ring(int dt, bool vec, const RingArgs& a, int grid, cudaStream_t s);
+cudaError_t ring_occupancy(int dt, bool vec, int proto, int* max_blocks_per_sm);
+cudaError_t launch_ring(int dt, bool vec, int proto, const RingArgs& a, int grid, cudaStream_t s);
 
 cudaError_t launch_ll_pack(const LLArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_ll_unpack(int dt, const LLArgs& a, int grid, cudaStream_t s);

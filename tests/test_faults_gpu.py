@@ -22,11 +22,14 @@ def _init():
     rra.rra_set_timeout_ns(0)
 
 
-@pytest.mark.parametrize("algo", [rra.RRA_ALGO_RING, rra.RRA_ALGO_TWO_SHOT])
+@pytest.mark.parametrize("algo,proto", [(rra.RRA_ALGO_RING, "simple"), (rra.RRA_ALGO_RING, "ll"),
+                                        (rra.RRA_ALGO_TWO_SHOT, None)])
 @pytest.mark.parametrize("skip", [0, 3])
-def test_crashed_rank_times_out_and_gpu_stays_usable(algo, skip):
+def test_crashed_rank_times_out_and_gpu_stays_usable(algo, proto, skip, monkeypatch):
     import gpu_util as g
 
+    if proto:
+        monkeypatch.setenv("RRA_RING_PROTO", proto)
     n, count = 4, 1 << 20
     xs = inputs.make_ranks(n, count, "float32", "normal", seed=1)
     ins = [g.to_dev(x, "float32") for x in xs]

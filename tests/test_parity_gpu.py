@@ -134,6 +134,40 @@ def test_order_sensitive_float_data(algo, dtype, n):
         _check(got[r], want[r], dtype, "%s n=%d r=%d" % (algo, n, r))
 
 
+@pytest.mark.parametrize("proto", ["simple", "ll"])
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n,count", [(2, 3), (3, 1001), (5, 70_001), (8, 8 * 4096 * 6 + 5), (8, 2_000_000)])
+def test_ring_link_protocols(proto, dtype, n, count, monkeypatch):
+    # the ring with Simple (fence + head flag) or LL (flag in every line)
+    # links: same bits as the oracle's ring, for all three ring operations
+    monkeypatch.setenv("RRA_RING_PROTO", proto)
+    g = G()
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=count + n)
+    for rep in range(2):
+        got = run_allreduce(xs, dtype, "ring")
+        want, _, _ = oracle.allreduce("ring", xs, dtype)
+        for r in range(n):
+            _check(got[r], want[r], dtype, "%s ring n=%d r=%d rep=%d" % (proto, n, r, rep))
+    rc = max(1, count // n)
+    xs = inputs.make_ranks(n, n * rc, dtype, dist, seed=rc)
+    ins = [g.to_dev(x, dtype) for x in xs]
+    outs = g.empty(n, rc, dtype)
+    rra.rra_reduce_scatter(ins, outs, rc, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_RING)
+    _status_ok()
+    want, _, _ = oracle.reduce_scatter("ring", xs, dtype)
+    for r in range(n):
+        _check(g.to_host(outs[r], dtype), want[r], dtype, "%s ring rs r=%d" % (proto, r))
+    shards = [x[:rc].copy() for x in xs]
+    ins = [g.to_dev(x, dtype) for x in shards]
+    outs = g.empty(n, n * rc, dtype)
+    rra.rra_all_gather(ins, outs, rc, g.CODE[dtype], rra.RRA_ALGO_RING)
+    _status_ok()
+    want, _, _ = oracle.all_gather("ring", shards, dtype)
+    for r in range(n):
+        _check(g.to_host(outs[r], dtype), want[r], dtype, "%s ring ag r=%d" % (proto, r))
+
+
 @pytest.mark.parametrize("algo", list(AR))
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("count", [1, 3, 4, 5, 8, 9, 17, 31, 100, 1001, 65537])
