@@ -55,7 +55,7 @@ def _load():
     vpp = ctypes.POINTER(ctypes.c_void_p)
     u64p = ctypes.POINTER(ctypes.c_uint64)
     szp = ctypes.POINTER(ctypes.c_size_t)
-    for name in ("orc_allreduce_ring", "orc_allreduce_oneshot", "orc_allreduce_twoshot",
+    for name in ("orc_allreduce_ring", "orc_allreduce_oneshot", "orc_allreduce_twoshot", "orc_allreduce_tree",
                  "orc_reduce_scatter_ring", "orc_reduce_scatter_direct",
                  "orc_all_gather_ring", "orc_all_gather_direct"):
         f = getattr(lib, name)
@@ -118,12 +118,12 @@ def _run(fname, xs, out_count, dtype):
 
 def allreduce(algo: str, xs, dtype: str):
     """All-reduce (SUM) of the n arrays in ``xs`` with schedule ``algo``
-    ("ring", "oneshot", "twoshot").  Returns (outs, sent, recv) where sent and
+    ("ring", "oneshot", "twoshot", "tree").  Returns (outs, sent, recv) where sent and
     recv are per-rank byte counters."""
     count = int(xs[0].size)
     outs, sent, recv, pin, pout = _run(None, xs, count, dtype)
     fn = {"ring": "orc_allreduce_ring", "oneshot": "orc_allreduce_oneshot",
-          "twoshot": "orc_allreduce_twoshot"}[algo]
+          "twoshot": "orc_allreduce_twoshot", "tree": "orc_allreduce_tree"}[algo]
     rc = getattr(_load(), fn)(len(xs), count, DTYPES[dtype], pin, pout, sent, recv)
     if rc != 0:
         raise RuntimeError("oracle %s failed: %d" % (fn, rc))

@@ -582,3 +582,57 @@ int orc_allreduce_rmsnorm(int n, size_t rows, size_t hidden, int dt, const void*
   free(y);
   return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* tree all-reduce                                                          */
+/* ------------------------------------------------------------------------ */
+
+/* "Collective communication: NCCL's algorithms and protocols, ...",
+ * section "Algorithms": tree -- reduce up the tree, then broadcast down it,
+ * in O(log n) steps.  The page does not fix the tree's shape or the order a
+ * node adds its inputs; the reading taken: one binary tree in heap order
+ * (parent of rank r is (r-1)/2, children 2r+1 and 2r+2), and a node's
+ * partial is its own data, then its left child's partial, then its right
+ * child's: p_r = (x_r (+) p_{2r+1}) (+) p_{2r+2}, missing children
+ * skipped.  Rank 0 holds the total; the broadcast hands it down unchanged,
+ * so every rank gets the same bits.  Byte counters: each non-root rank
+ * sends its partial up once and receives the result once; each parent
+ * receives one partial per child and sends the result once per child. */
+int orc_allreduce_tree(int n, size_t count, int dt, const void* const* in, void* const* out,
+                       uint64_t* sent, uint64_t* recv) {
+  if (n < 1 || n > 64) return ORC_EINVAL;
+  size_t e = elem_size(dt);
+  void** part = (void**)calloc((size_t)n, sizeof(void*));
+  if (!part) return ORC_ENOMEM;
+  int rc = ORC_OK;
+  for (int r = 0; r < n; ++r) {
+    part[r] = malloc(count * 4 + 4);
+    if (!part[r]) { rc = ORC_ENOMEM; goto done; }
+  }
+  /* reduce up: children have larger indices, so descending order finishes
+   * every child before its parent */
+  for (int r = n - 1; r >= 0; --r) {
+    acc_load(dt, in[r], 0, count, part[r]);
+    for (int child = 2 * r + 1; child <= 2 * r + 2; ++child) {
+      if (child >= n) continue;
+      tally(sent, child, count * e);
+      tally(recv, r, count * e);
+      if (dt == ORC_INT32)
+        for (size_t i = 0; i < count; ++i) ((uint32_t*)part[r])[i] += ((uint32_t*)part[child])[i];
+      else
+        for (size_t i = 0; i < count; ++i) ((float*)part[r])[i] = ((float*)part[r])[i] + ((float*)part[child])[i];
+    }
+  }
+  /* broadcast down: the root's rounded total, forwarded unchanged */
+  acc_store(dt, part[0], out[0], 0, count);
+  for (int r = 1; r < n; ++r) {
+    int parent = (r - 1) / 2;
+    memcpy(out[r], out[parent], count * e);
+    tally(sent, parent, count * e);
+    tally(recv, r, count * e);
+  }
+done:
+  for (int r = 0; r < n; ++r) free(part[r]);
+  free(part);
+  return rc;
+}
