@@ -40,6 +40,7 @@ RRA_ALGO_ONE_SHOT = 2
 RRA_ALGO_TWO_SHOT = 3
 RRA_ALGO_DIRECT = 4
 RRA_ALGO_COPY_ENGINE = 5
+RRA_ALGO_TREE = 6
 
 RRA_MAX_RANKS = 8
 

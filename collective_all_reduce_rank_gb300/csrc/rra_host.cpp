@@ -83,6 +83,7 @@ const char* algo_name(int a) {
     case RRA_ALGO_TWO_SHOT: return "two_shot";
     case RRA_ALGO_DIRECT: return "direct";
     case RRA_ALGO_COPY_ENGINE: return "copy_engine";
+    case RRA_ALGO_TREE: return "tree";
     default: return "?";
   }
 }
@@ -93,6 +94,7 @@ int parse_algo(const char* s) {
   if (!std::strcmp(s, "one_shot") || !std::strcmp(s, "oneshot")) return RRA_ALGO_ONE_SHOT;
   if (!std::strcmp(s, "two_shot") || !std::strcmp(s, "twoshot")) return RRA_ALGO_TWO_SHOT;
   if (!std::strcmp(s, "direct")) return RRA_ALGO_DIRECT;
+  if (!std::strcmp(s, "tree")) return RRA_ALGO_TREE;
   return -1;
 }
 
@@ -224,6 +226,38 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
     a.chunk_lo[c] = lo;
     a.chunk_len[c] = hi - lo;
   }
+  a.wait = wait_cfg(s);
+  // Cluster form (TMA staging, exchange through distributed shared memory)
+  // for aligned buffers; not with fault injection, whose silent rank would
+  // leave its cluster peers at a hardware barrier.
+  if (vec && n >= 2 && a.wait.skip_rank < 0 && env_long("RRA_TWOSHOT_CLUSTER", 1) != 0) {
+    const int maxc = twoshot_cluster_max_clusters(n, dt);
+    if (maxc > 0) {
+      const size_t tu = (size_t)twoshot_cluster_tile_bytes(n) / 16;
+      const size_t units0 = a.chunk_len[0] / pu;
+      long c = std::min<long>({(long)maxc, (long)std::max<size_t>(1, (units0 + tu - 1) / tu), channel_cap(n)});
+      c = std::min(c, env_long("RRA_TWOSHOT_CHANNELS", c));
+      a.channels = (int)std::max(1L, c);
+      *grid_out = n * a.channels;
+      cudaError_t err = launch_twoshot_cluster(n, dt, a, n * a.channels, st);
+      // the sub-unit tail of the last chunk (fewer than 16 bytes): same
+      // ascending sum by the one-shot kernel
+      size_t tail_lo = count;
+      for (int c2 = 0; c2 < n; ++c2)
+        if (a.chunk_len[c2] % pu) tail_lo = a.chunk_lo[c2] + a.chunk_len[c2] / pu * pu;
+      if (err == cudaSuccess && tail_lo < count) {
+        DirectArgs t{};
+        for (int r = 0; r < n; ++r) {
+          t.in[r] = static_cast<const char*>(in[r]) + tail_lo * e;
+          t.out[r] = static_cast<char*>(out[r]) + tail_lo * e;
+        }
+        t.count = count - tail_lo;
+        int g2 = 0;
+        err = launch_oneshot(n, dt, false, t, 1, &g2, st);
+      }
+      return cuda_status(err);
+    }
+  }
   a.tile_units = kDirectThreads * kTwoShotUnitsPerThread;
   int occ = 0;
   cudaError_t err = twoshot_occupancy(n, dt, vec, &occ);
@@ -269,6 +303,48 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   }
   a.n = n;
   a.mode = mode;
+  a.wait = wait_cfg(s);
+  // Cluster form: the ring's links in distributed shared memory, tiles by
+  // bulk copies.  It needs 16-byte aligned buffers and chunk starts, whole
+  // units in every chunk but the last, and no fault injection (a silent
+  // rank would leave its cluster at a hardware barrier).
+  bool cluster_ok = vec && n >= 2 && a.wait.skip_rank < 0 && env_long("RRA_RING_CLUSTER", 1) != 0;
+  for (int c = 0; c < n && cluster_ok; ++c) {
+    cluster_ok = (ibase[c] * e) % 16 == 0 && (obase[c] * e) % 16 == 0;
+    if (c + 1 < n && len[c] % pu) cluster_ok = cluster_ok && mode == kRingAllReduce && len[c + 1] == 0;
+  }
+  if (cluster_ok && mode != kRingAllReduce)
+    for (int c = 0; c < n; ++c) cluster_ok = cluster_ok && len[c] % pu == 0;
+  const int maxc = cluster_ok ? ring_cluster_max_clusters(n, dt) : 0;
+  if (maxc > 0) {
+    a.G = (int)std::max(1L, std::min((long)ring_cluster_slots(dt) / 2, env_long("RRA_RING_G", ring_cluster_slots(dt) / 2)));
+    a.K = ring_cluster_slots(dt);
+    const size_t tu = (size_t)ring_cluster_tile_units(dt);
+    size_t wmax = 0;
+    for (int c = 0; c < n; ++c) wmax = std::max(wmax, len[c] / pu);
+    const size_t need = (wmax + (size_t)a.G * tu - 1) / ((size_t)a.G * tu);
+    long c = std::min<long>({(long)maxc, (long)std::max<size_t>(1, need), channel_cap(n)});
+    c = std::min(c, env_long("RRA_RING_CHANNELS", c));
+    a.channels = (int)std::max(1L, c);
+    *grid_out = n * a.channels;
+    cudaError_t err = launch_ring_cluster(dt, a, n * a.channels, st);
+    // sub-unit tail of the ragged chunk: the ring's order for that chunk,
+    // x_{c+1}, ..., x_{c-1}, x_c, by the one-shot kernel on rotated inputs
+    for (int c = 0; c < n && err == cudaSuccess; ++c) {
+      if (len[c] % pu == 0) continue;
+      const size_t done = len[c] / pu * pu;
+      DirectArgs t{};
+      for (int k = 0; k < n; ++k) {
+        const int src = (c + 1 + k) % n;
+        t.in[k] = static_cast<const char*>(in[src]) + (ibase[c] + done) * e;
+        t.out[k] = static_cast<char*>(out[k]) + (obase[c] + done) * e;
+      }
+      t.count = len[c] - done;
+      int g2 = 0;
+      err = launch_oneshot(n, dt, false, t, 1, &g2, st);
+    }
+    return cuda_status(err);
+  }
   a.slice_units = kRingThreads * kRingUnitsPerThread;
   const int proto = ring_proto(maxu * 16);
   // Credits: a rank's sends minus receives never exceed G.  Simple raises a
@@ -448,12 +524,17 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
                            rra_dtype_t dtype, rra_op_t op, rra_algo_t algo, rra_stream_t stream) {
   const char* call = "allreduce";
   if (!bufs || !outs || nranks < 1 || !valid_dtype(dtype) || op != RRA_SUM || (int)algo < 0 ||
-      (int)algo > RRA_ALGO_TWO_SHOT)
+      ((int)algo > RRA_ALGO_TWO_SHOT && algo != RRA_ALGO_TREE))
     return record(call, algo, nranks, count, dtype, 0,
                   nranks > kMaxRanks ? RRA_ERR_UNSUPPORTED : RRA_ERR_INVALID_ARG);
   if (nranks > kMaxRanks) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_UNSUPPORTED);
   const size_t e = elem_size(dtype);
   if (count > (SIZE_MAX / 2) / e) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_INVALID_ARG);
+  if (algo == RRA_ALGO_TREE && nranks > 1) {
+    for (int r = 0; r < nranks; ++r)
+      if (!bufs[r] || !outs[r] || !aligned(bufs[r], 16) || !aligned(outs[r], 16))
+        return record(call, algo, nranks, count, dtype, 0, RRA_ERR_UNSUPPORTED);
+  }
   for (int r = 0; r < nranks; ++r)
     if (!bufs[r] || !outs[r] || !aligned(bufs[r], e) || !aligned(outs[r], e))
       return record(call, algo, nranks, count, dtype, 0, RRA_ERR_INVALID_ARG);
@@ -462,7 +543,8 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
   if (al != RRA_SUCCESS) return record(call, algo, nranks, count, dtype, 0, al);
   if (algo == RRA_ALGO_AUTO) {
     const int env = parse_algo(std::getenv("RRA_ALGO"));
-    algo = (env == RRA_ALGO_RING || env == RRA_ALGO_ONE_SHOT || env == RRA_ALGO_TWO_SHOT)
+    algo = (env == RRA_ALGO_RING || env == RRA_ALGO_ONE_SHOT || env == RRA_ALGO_TWO_SHOT ||
+            (env == RRA_ALGO_TREE && all_aligned16(bufs, nranks) && all_aligned16((const void* const*)outs, nranks)))
                ? (rra_algo_t)env
                : rra_select_algo(nranks, S, dtype);
   }
@@ -518,7 +600,17 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
   if (!s || !s->ready) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_NOT_INITIALIZED);
   int grid = 0;
   rra_status_t rs;
-  if (algo == RRA_ALGO_TWO_SHOT) {
+  if (algo == RRA_ALGO_TREE) {
+    const int maxc = tree_max_clusters(nranks, dtype);
+    if (maxc <= 0) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_UNSUPPORTED);
+    const int G = (int)std::max(1L, std::min(4L, env_long("RRA_TREE_G", 2)));
+    const size_t tu = (size_t)tree_tile_units_for(dtype);
+    const size_t tiles = (count * e / 16 + tu - 1) / tu;
+    long c = std::min<long>({(long)maxc, (long)std::max<size_t>(1, (tiles + G - 1) / G), channel_cap(nranks)});
+    c = std::min(c, env_long("RRA_TREE_CHANNELS", c));
+    grid = nranks * (int)std::max(1L, c);
+    rs = cuda_status(launch_tree(dtype, bufs, outs, nranks, count, (int)std::max(1L, c), G, wait_cfg(s), st));
+  } else if (algo == RRA_ALGO_TWO_SHOT) {
     rs = run_twoshot(s, bufs, outs, nranks, count, dtype, vec, st, &grid);
   } else {
     const size_t pu = 16 / e;

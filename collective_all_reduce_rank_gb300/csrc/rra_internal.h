@@ -163,6 +163,26 @@ cudaError_t launch_allreduce_rmsnorm(int n, int dt, bool vec, const void* const*
 // the launch fails.  *max_blocks_per_sm reports the occupancy limit.
 cudaError_t twoshot_occupancy(int n, int dt, bool vec, int* max_blocks_per_sm);
 cudaError_t launch_twoshot(int n, int dt, bool vec, const TwoShotArgs& a, int grid, cudaStream_t s);
+// Two-shot on thread-block clusters of n CTAs (n in [2, 8]): whole 16-byte
+// units, 16-byte aligned buffers; grid = n * clusters.
+int twoshot_cluster_tile_bytes(int n);
+int twoshot_cluster_max_clusters(int n, int dt);
+cudaError_t launch_twoshot_cluster(int n, int dt, const TwoShotArgs& a, int grid, cudaStream_t s);
+
+// Ring on thread-block clusters of n CTAs: whole 16-byte units, 16-byte
+// aligned chunk starts; a.G tiles per step (< the compiled slot count).
+int ring_cluster_tile_units(int dt);
+int ring_cluster_slots(int dt);
+int ring_cluster_max_clusters(int n, int dt);
+cudaError_t launch_ring_cluster(int dt, const RingArgs& a, int grid, cudaStream_t s);
+
+// Tree all-reduce on thread-block clusters of n CTAs (16-byte aligned
+// buffers): `channels` clusters, G tiles per batch (G <= 4).
+int tree_tile_units_for(int dt);
+int tree_max_clusters(int n, int dt);
+cudaError_t launch_tree(int dt, const void* const* in, void* const* out, int n, size_t count, int channels, int G,
+                        const WaitCfg& w, cudaStream_t s);
+
 cudaError_t ring_occupancy(int dt, bool vec, int proto, int* max_blocks_per_sm);
 cudaError_t launch_ring(int dt, bool vec, int proto, const RingArgs& a, int grid, cudaStream_t s);
 

@@ -83,7 +83,12 @@ typedef enum {
   /** all-gather only: the GPU's copy engines move the shards
    *  (cudaMemcpyAsync device to device), no SM runs a kernel ([AIH]
    *  "Protocols": transfer methods that use no SMs, like the copy engine). */
-  RRA_ALGO_COPY_ENGINE = 5
+  RRA_ALGO_COPY_ENGINE = 5,
+  /** all-reduce only: reduce up a binary tree, broadcast down it ([AIH]
+   *  "Algorithms": tree, O(log n) steps).  Heap order (parent of r is
+   *  (r-1)/2); node r sums its own data, then its left child's partial,
+   *  then its right child's.  Needs 16-byte aligned buffers. */
+  RRA_ALGO_TREE = 6
 } rra_algo_t;
 
 /* ------------------------------------------------------------------------ */

@@ -134,13 +134,20 @@ def test_order_sensitive_float_data(algo, dtype, n):
         _check(got[r], want[r], dtype, "%s n=%d r=%d" % (algo, n, r))
 
 
-@pytest.mark.parametrize("proto", ["simple", "ll"])
+@pytest.mark.parametrize("path", ["cluster", "simple", "ll"])
 @pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
-@pytest.mark.parametrize("n,count", [(2, 3), (3, 1001), (5, 70_001), (8, 8 * 4096 * 6 + 5), (8, 2_000_000)])
-def test_ring_link_protocols(proto, dtype, n, count, monkeypatch):
-    # the ring with Simple (fence + head flag) or LL (flag in every line)
-    # links: same bits as the oracle's ring, for all three ring operations
-    monkeypatch.setenv("RRA_RING_PROTO", proto)
+@pytest.mark.parametrize("n,count", [(2, 3), (3, 1001), (5, 70_001), (8, 8 * 4096 * 6 + 5), (8, 2_000_000),
+                                     (4, 3 * 2048 * 8 * 4)])
+def test_ring_link_protocols(path, dtype, n, count, monkeypatch):
+    # the ring on a thread-block cluster (links in distributed shared
+    # memory), or per-warp with Simple (fence + head flag) or LL (flag in
+    # every line) links in L2: same bits as the oracle's ring, for all three
+    # ring operations
+    if path == "cluster":
+        monkeypatch.setenv("RRA_RING_CLUSTER", "1")
+    else:
+        monkeypatch.setenv("RRA_RING_CLUSTER", "0")
+        monkeypatch.setenv("RRA_RING_PROTO", path)
     g = G()
     dist = "int20" if dtype == "int32" else "normal"
     xs = inputs.make_ranks(n, count, dtype, dist, seed=count + n)
@@ -166,6 +173,22 @@ def test_ring_link_protocols(proto, dtype, n, count, monkeypatch):
     want, _, _ = oracle.all_gather("ring", shards, dtype)
     for r in range(n):
         _check(g.to_host(outs[r], dtype), want[r], dtype, "%s ring ag r=%d" % (proto, r))
+
+
+@pytest.mark.parametrize("cluster", ["0", "1"])
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n,count", [(2, 5), (3, 4099), (8, 8 * 2048 * 19 * 3 + 11), (8, 1_000_003), (7, 777_777)])
+def test_two_shot_cluster_and_warp_forms(cluster, dtype, n, count, monkeypatch):
+    # two-shot on a thread-block cluster (exchange through distributed
+    # shared memory) and the per-warp form with flags in L2: same bits
+    monkeypatch.setenv("RRA_TWOSHOT_CLUSTER", cluster)
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=count)
+    want, _, _ = oracle.allreduce("twoshot", xs, dtype)
+    for inplace in (False, True):
+        got = run_allreduce(xs, dtype, "twoshot", inplace=inplace)
+        for r in range(n):
+            _check(got[r], want[r], dtype, "cluster=%s n=%d r=%d inplace=%s" % (cluster, n, r, inplace))
 
 
 @pytest.mark.parametrize("algo", list(AR))

@@ -1,0 +1,67 @@
+"""Tree all-reduce on the GPU vs the oracle's tree, bit for bit."""
+import numpy as np
+import pytest
+
+import oracle
+import collective_all_reduce_rank_gb300 as rra
+from collective_all_reduce_rank_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _init():
+    import torch
+
+    torch.cuda.set_device(0)
+    rra.rra_init(0)
+    rra.rra_set_timeout_ns(2_000_000_000)
+    yield
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 7, 8])
+@pytest.mark.parametrize("count", [1, 7, 4096, 100_003, 3_000_001])
+def test_tree_matches_oracle(dtype, n, count):
+    import gpu_util as g
+
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=count + n)
+    want, _, _ = oracle.allreduce("tree", xs, dtype)
+    for inplace in (False, True):
+        ins = [g.to_dev(x, dtype) for x in xs]
+        outs = ins if inplace else g.empty(n, count, dtype)
+        rra.rra_allreduce(ins, outs, count, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_TREE)
+        st, info = rra.rra_query_status()
+        assert st == 0, info
+        for r in range(n):
+            got = g.to_host(outs[r], dtype)
+            if dtype == "bfloat16":
+                assert g.bf16_rel_ok(got, want[r])
+            g.assert_bits_equal(got, want[r], "tree n=%d r=%d inplace=%s" % (n, r, inplace))
+
+
+def test_tree_order_case_on_gpu():
+    # the hand-derived n = 4 case of the oracle's pins: (0, 1.5) per column
+    import gpu_util as g
+
+    B = float(2 ** 25)
+    cols = np.array([[0.5, 0.5], [B, B], [-B, 1.0], [0.0, -B]], np.float32)
+    xs = [np.tile(c, 2048) for c in cols]  # several tiles
+    ins = [g.to_dev(x, "float32") for x in xs]
+    outs = g.empty(4, xs[0].size, "float32")
+    rra.rra_allreduce(ins, outs, xs[0].size, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE)
+    assert rra.rra_query_status()[0] == 0
+    for r in range(4):
+        got = g.to_host(outs[r], "float32").reshape(-1, 2)
+        assert np.all(got[:, 0] == 0.0) and np.all(got[:, 1] == 1.5)
+
+
+def test_tree_rejects_unaligned():
+    import gpu_util as g
+
+    xs = inputs.make_ranks(2, 1001, "float32", "normal")
+    ins = [g.to_dev(np.concatenate([[0.0], x]).astype(np.float32), "float32")[1:] for x in xs]
+    outs = g.empty(2, 1001, "float32")
+    st = rra.rra_allreduce(ins, outs, 1001, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE, check=False)
+    assert st == rra.RRA_ERR_UNSUPPORTED
