@@ -373,6 +373,8 @@ def run_ours(args):
         "clocks": clk.summary(),
         "parity_sample_ok": parity,
     }
+    if not args.no_next:
+        line["next_rows"] = next_rows(torch, rra, inputs, step, stream)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_scale or 2)
     if args.small:
@@ -380,6 +382,61 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def time_op(torch, fn, stream, reps=10):
+    """Median milliseconds of fn() on `stream` (CUDA events, after warm-up)."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def next_rows(torch, rra, inputs, step, stream):
+    """The rows beyond the step's hot path, each timed on its own: the tree
+    all-reduce of the bucket, all-reduce + RMSNorm of the 512-token
+    activations, the copy-engine all-gather, and GB/s against the SM budget."""
+    n, S = N_RANKS, step.count * 4
+    F, SUM = rra.RRA_FLOAT32, rra.RRA_SUM
+    out = {}
+    ms = time_op(torch, lambda: rra.rra_allreduce(step.x, step.ar_out, step.count, F, SUM, rra.RRA_ALGO_TREE,
+                                                 stream), stream)
+    out["ar_tree_bucket"] = {"ms": round(ms, 4), "GBps": round(2 * n * S / ms / 1e6, 1),
+                             "busbw": round(S / ms / 1e6 * bus_factor("ar_", n), 1)}
+    ms = time_op(torch, lambda: rra.rra_all_gather(step.sh, step.ag_out, step.rc, F, rra.RRA_ALGO_COPY_ENGINE,
+                                                   stream), stream)
+    out["ag_copy_engine_bucket"] = {"ms": round(ms, 4), "GBps": round((n + 1) * S / ms / 1e6, 1)}
+    t, h = 512, inputs.TP_HIDDEN
+    xs = inputs.cfg_tp_activations(t)
+    ins = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
+    outs = [torch.empty_like(x) for x in ins]
+    gamma = torch.ones(h, dtype=torch.bfloat16, device="cuda")
+    ms = time_op(torch, lambda: rra.rra_allreduce_rmsnorm(ins, outs, gamma, h, 1e-6, stream=stream), stream, 50)
+    ms_ar = time_op(torch, lambda: rra.rra_allreduce(ins, outs, t * h, rra.RRA_BFLOAT16, SUM,
+                                                    rra.RRA_ALGO_ONE_SHOT, stream), stream, 50)
+    out["ar_rmsnorm_tp512"] = {"us": round(ms * 1e3, 2), "one_shot_ar_only_us": round(ms_ar * 1e3, 2)}
+    budget = {}
+    for ctas in (16, 32, 64, 152, 0):
+        rra.rra_set_max_ctas(ctas)
+        row = {}
+        for name, algo in (("one_shot", rra.RRA_ALGO_ONE_SHOT), ("two_shot", rra.RRA_ALGO_TWO_SHOT)):
+            ms = time_op(torch, lambda: rra.rra_allreduce(step.x, step.ar_out, step.count, F, SUM, algo, stream),
+                         stream, 5)
+            row[name] = round(2 * n * S / ms / 1e6, 1)
+        budget["all" if ctas == 0 else str(ctas)] = row
+    rra.rra_set_max_ctas(0)
+    out["sm_budget_GBps"] = budget
+    return out
 
 
 def max_over_ranks(values, dist, device):
@@ -684,6 +741,7 @@ def main():
     ap.add_argument("--profile", default=None, help="run these ops once (comma list or 'all') and exit")
     ap.add_argument("--scale", type=int, default=4, help="workload fraction for --profile")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the rows beyond the step (tree, RMSNorm, ...)")
     ap.add_argument("--small", action="store_true", help="add the TP-activation latency table")
     ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")
     ap.add_argument("--sweep-max", type=int, default=1 << 30)

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kCRingThreads, 1) ring_cluster_kernel(const __
   if (tid == 0) {
     for (int i = 0; i < XS; ++i) c_mbar_init(&x_full[i], 1);
     for (int j = 0; j < K; ++j) {
-      c_mbar_init(&r_full[j], 1);
+      c_mbar_init(&r_full[j], 2);  // the receiver's arm + the sender's arrival
       c_mbar_init(&s_free[j], 1);
     }
     s_fail = 0;
@@ -244,9 +244,14 @@ __global__ void __launch_bounds__(kCRingThreads, 1) ring_cluster_kernel(const __
             c_bulk_store(y, so, nu * 16u);
             c_bulk_commit();
           }
-          if (send && nu > 0) {
-            const uint32_t bytes = nu * 16u * (partial_out ? AW : 1);
-            c_bulk_push(peer_addr(rslot + (size_t)jout * TU * AW, next), so, bytes, peer_addr(&r_full[jout], next));
+          if (send) {
+            if (nu > 0) {
+              const uint32_t bytes = nu * 16u * (partial_out ? AW : 1);
+              c_bulk_push(peer_addr(rslot + (size_t)jout * TU * AW, next), so, bytes, peer_addr(&r_full[jout], next));
+            }
+            // the sender's arrival, also for an empty tile: the receiver never
+            // consumes (and credits) a message its sender has not reached
+            c_mbar_remote_arrive(peer_addr(&r_full[jout], next));
           }
           if (recv) {
             arm_recv(m_in + K);  // before the credit: the next push into this slot finds it armed

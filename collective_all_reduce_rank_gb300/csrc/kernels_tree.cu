@@ -149,10 +149,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_cluster_kernel(const __g
   if (tid == 0) {
     for (int i = 0; i < XS; ++i) c_mbar_init(&x_full[i], 1);
     for (int j = 0; j < K; ++j) {
-      c_mbar_init(&u_full[0][j], 1);
-      c_mbar_init(&u_full[1][j], 1);
+      c_mbar_init(&u_full[0][j], 2);  // the receiver's arm + the sender's arrival
+      c_mbar_init(&u_full[1][j], 2);
       c_mbar_init(&u_free[j], 1);
-      c_mbar_init(&d_full[j], 1);
+      c_mbar_init(&d_full[j], 2);
       c_mbar_init(&d_free[0][j], 1);
       c_mbar_init(&d_free[1][j], 1);
     }
@@ -242,19 +242,26 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_cluster_kernel(const __g
       }
       __syncthreads();
       if (tid == 0 && !s_fail) {
-        if (nu > 0) {
-          if (r > 0) {
+        // every message, empty or not, ends with the sender's arrival on the
+        // receiver's barrier: no receiver runs ahead of its sender
+        if (r > 0) {
+          if (nu > 0)
             c_bulk_push(peer_addr(urecv + ((size_t)side * K + j) * TU * AW, parent), usend + (size_t)j * TU * AW,
                         nu * 16u * AW, peer_addr(&u_full[side][j], parent));
-          } else {
-            uint4* src = dsend + (size_t)j * TU;
+          c_mbar_remote_arrive(peer_addr(&u_full[side][j], parent));
+        } else {
+          uint4* src = dsend + (size_t)j * TU;
+          if (nu > 0) {
             c_bulk_store(static_cast<char*>(a.out[0]) + t * (size_t)T, src, nu * 16u);
             c_bulk_commit();
-            for (int s = 0; s < 2; ++s)
-              if (has_kid[s])
+          }
+          for (int s = 0; s < 2; ++s)
+            if (has_kid[s]) {
+              if (nu > 0)
                 c_bulk_push(peer_addr(drecv + (size_t)j * TU, 2 * r + 1 + s), src, nu * 16u,
                             peer_addr(&d_full[j], 2 * r + 1 + s));
-          }
+              c_mbar_remote_arrive(peer_addr(&d_full[j], 2 * r + 1 + s));
+            }
         }
         // children's slots used: re-arm for the message K later, give credits
         for (int s = 0; s < 2; ++s) {
@@ -293,11 +300,14 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_cluster_kernel(const __g
         if (nu > 0) {
           c_bulk_store(static_cast<char*>(a.out[r]) + t * (size_t)T, src, nu * 16u);
           c_bulk_commit();
-          for (int s = 0; s < 2; ++s)
-            if (has_kid[s])
+        }
+        for (int s = 0; s < 2; ++s)
+          if (has_kid[s]) {
+            if (nu > 0)
               c_bulk_push(peer_addr(drecv + (size_t)j * TU, 2 * r + 1 + s), src, nu * 16u,
                           peer_addr(&d_full[j], 2 * r + 1 + s));
-        }
+            c_mbar_remote_arrive(peer_addr(&d_full[j], 2 * r + 1 + s));
+          }
         if (md + K < total) c_mbar_arrive_tx(&d_full[j], tile_units(msg_tile(md + K)) * 16u);
         c_mbar_remote_arrive(peer_addr(&d_free[side][j], parent));
         if (nu > 0) c_bulk_wait_read0();

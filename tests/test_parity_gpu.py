@@ -155,7 +155,7 @@ def test_ring_link_protocols(path, dtype, n, count, monkeypatch):
         got = run_allreduce(xs, dtype, "ring")
         want, _, _ = oracle.allreduce("ring", xs, dtype)
         for r in range(n):
-            _check(got[r], want[r], dtype, "%s ring n=%d r=%d rep=%d" % (proto, n, r, rep))
+            _check(got[r], want[r], dtype, "%s ring n=%d r=%d rep=%d" % (path, n, r, rep))
     rc = max(1, count // n)
     xs = inputs.make_ranks(n, n * rc, dtype, dist, seed=rc)
     ins = [g.to_dev(x, dtype) for x in xs]
@@ -164,7 +164,7 @@ def test_ring_link_protocols(path, dtype, n, count, monkeypatch):
     _status_ok()
     want, _, _ = oracle.reduce_scatter("ring", xs, dtype)
     for r in range(n):
-        _check(g.to_host(outs[r], dtype), want[r], dtype, "%s ring rs r=%d" % (proto, r))
+        _check(g.to_host(outs[r], dtype), want[r], dtype, "%s ring rs r=%d" % (path, r))
     shards = [x[:rc].copy() for x in xs]
     ins = [g.to_dev(x, dtype) for x in shards]
     outs = g.empty(n, n * rc, dtype)
@@ -172,7 +172,7 @@ def test_ring_link_protocols(path, dtype, n, count, monkeypatch):
     _status_ok()
     want, _, _ = oracle.all_gather("ring", shards, dtype)
     for r in range(n):
-        _check(g.to_host(outs[r], dtype), want[r], dtype, "%s ring ag r=%d" % (proto, r))
+        _check(g.to_host(outs[r], dtype), want[r], dtype, "%s ring ag r=%d" % (path, r))
 
 
 @pytest.mark.parametrize("cluster", ["0", "1"])
