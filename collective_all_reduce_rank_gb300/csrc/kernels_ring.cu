@@ -213,12 +213,46 @@ struct RingWarp {
     }
   }
 
+  // The rank's own input for the next message that reads it is loaded one
+  // such message ahead, so its HBM latency overlaps the current message.
+  // Those messages come in a fixed order: per iteration, the reduce-scatter
+  // sends k = 0..n-2 (chunk r-k-1) and the final step (chunk r), G slices
+  // each; in all-gather mode only the own shard.
+  uint4 xn[UPT];
+  int vn[UPT];
+  uint64_t xq = 0, xq_total = 0;
+  int ch_ = 0;
+  size_t wofs_ = 0;
+
+  __device__ __forceinline__ void prefetch_x() {
+    if (xq >= xq_total) return;
+    const int n = a.n, G = a.G;
+    const int XK = a.mode == kRingAllGather ? 1 : n;
+    const uint64_t per = (uint64_t)XK * G;
+    const size_t it = (size_t)(xq / per);
+    const int rem = (int)(xq % per);
+    const int k = rem / G, g = rem % G;
+    const int c = a.mode == kRingAllGather ? r : (k <= n - 2 ? ((r - k - 1) % n + n) % n : r);
+    const size_t base = (it * a.channels + ch_) * (size_t)G * a.slice_units + wofs_ + (size_t)g * a.slice_units;
+    load_x(c, base, xn, vn);
+  }
+
+  __device__ __forceinline__ void take_x(uint4* xv, int* v) {
+#pragma unroll
+    for (int j = 0; j < UPT; ++j) {
+      xv[j] = xn[j];
+      v[j] = vn[j];
+    }
+    ++xq;
+    prefetch_x();
+  }
+
   // Reduce-scatter send of chunk c (first step: own data; later steps:
   // received partial (+) own data).
   __device__ __forceinline__ bool rs_step(int c, bool first, size_t base, int step) {
     uint4 xv[UPT];
     int v[UPT];
-    load_x(c, base, xv, v);
+    take_x(xv, v);  // chunk c at base, loaded one message ago
     if (!wait(!first, true, step)) return false;
     uint4 p[UPT][2];
     if (!first && !get(slot_in(), v, AW, p, step)) return false;
@@ -247,7 +281,7 @@ struct RingWarp {
   __device__ __forceinline__ bool rs_final(size_t base, bool fwd, int step) {
     uint4 xv[UPT];
     int v[UPT];
-    load_x(r, base, xv, v);
+    take_x(xv, v);  // chunk r at base, loaded one message ago
     if (!wait(a.n > 1, fwd, step)) return false;
     uint4 p[UPT][2];
     if (a.n > 1 && !get(slot_in(), v, AW, p, step)) return false;
@@ -276,7 +310,7 @@ struct RingWarp {
   __device__ __forceinline__ bool ag_first(size_t base, int step) {
     uint4 xv[UPT];
     int v[UPT];
-    load_x(r, base, xv, v);
+    take_x(xv, v);  // chunk r at base, loaded one message ago
     if (!wait(false, true, step)) return false;
     char* y = static_cast<char*>(a.out[r]) + a.obase[r] * ES;
     char* so = slot_out();
@@ -323,6 +357,10 @@ struct RingWarp {
     const size_t per_iter = (size_t)C * G * slice;
     const size_t iters = (maxu + per_iter - 1) / per_iter;
     const size_t wofs = (size_t)warp * 32 * UPT;
+    ch_ = ch;
+    wofs_ = wofs;
+    xq_total = (uint64_t)iters * (a.mode == kRingAllGather ? 1 : n) * G;
+    prefetch_x();
     for (size_t it = 0; it < iters; ++it) {
       const size_t it_base = (it * C + ch) * G * slice + wofs;
       int step = 0;

@@ -35,25 +35,30 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
   const size_t per_iter = (size_t)C * tile;
   const size_t iters = ((a.chunk_len[0] + PU - 1) / PU + per_iter - 1) / per_iter;  // chunk 0 is the longest
   uint64_t* my_flag = a.progress + ((size_t)r * C + ch) * W + warp;
+  const size_t lo = a.chunk_lo[r] * ES;
+  const size_t len = a.chunk_len[r];
+  // The inputs of iteration it+1 are loaded right after iteration it's
+  // reduce, so their HBM latency overlaps the all-gather part of it.
+  uint4 x[UPT][N];
+  int v[UPT];
+  auto load_x = [&](size_t it) {
+    const size_t t0 = (it * C + ch) * tile + wofs;
+#pragma unroll
+    for (int j = 0; j < UPT; ++j) {
+      const size_t u = t0 + (size_t)j * 32 + lane;
+      v[j] = unit_valid<DT>(u, len);
+      if (v[j] > 0) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) x[j][k] = load_in<DT, VEC>(static_cast<const char*>(a.in[k]) + lo, u, v[j]);
+      }
+    }
+  };
+  if (iters > 0) load_x(0);
 
   for (size_t it = 0; it < iters; ++it) {
     const size_t t0 = (it * C + ch) * tile + wofs;
     // phase 1: reduce-scatter part
     {
-      const size_t lo = a.chunk_lo[r] * ES;
-      const size_t len = a.chunk_len[r];
-      uint4 x[UPT][N];
-      int v[UPT];
-#pragma unroll
-      for (int j = 0; j < UPT; ++j) {
-        const size_t u = t0 + (size_t)j * 32 + lane;
-        v[j] = unit_valid<DT>(u, len);
-        if (v[j] > 0) {
-#pragma unroll
-          for (int k = 0; k < N; ++k)
-            x[j][k] = load_in<DT, VEC>(static_cast<const char*>(a.in[k]) + lo, u, v[j]);
-        }
-      }
 #pragma unroll
       for (int j = 0; j < UPT; ++j) {
         if (v[j] > 0) {
@@ -68,6 +73,7 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
     }
     __syncwarp();
     if (lane == 0) st_release(my_flag, E | (uint64_t)(it + 1));
+    if (it + 1 < iters) load_x(it + 1);
 
     // phase 2: all-gather part.  Lane j waits for peer (r + j) mod N, so the
     // n-1 acquires run side by side; __syncwarp then orders every lane's

@@ -4,6 +4,7 @@
 // collectives runs in the kernels (kernels_*.cu); this file only decides
 // what to launch.
 #include <cuda_runtime.h>
+#include <dlfcn.h>
 
 #include <algorithm>
 #include <atomic>
@@ -230,7 +231,7 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
   // Cluster form (TMA staging, exchange through distributed shared memory)
   // for aligned buffers; not with fault injection, whose silent rank would
   // leave its cluster peers at a hardware barrier.
-  if (vec && n >= 2 && a.wait.skip_rank < 0 && env_long("RRA_TWOSHOT_CLUSTER", 1) != 0) {
+  if (vec && n >= 2 && a.wait.skip_rank < 0 && env_long("RRA_TWOSHOT_CLUSTER", 0) != 0) {
     const int maxc = twoshot_cluster_max_clusters(n, dt);
     if (maxc > 0) {
       const size_t tu = (size_t)twoshot_cluster_tile_bytes(n) / 16;
@@ -308,7 +309,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   // bulk copies.  It needs 16-byte aligned buffers and chunk starts, whole
   // units in every chunk but the last, and no fault injection (a silent
   // rank would leave its cluster at a hardware barrier).
-  bool cluster_ok = vec && n >= 2 && a.wait.skip_rank < 0 && env_long("RRA_RING_CLUSTER", 1) != 0;
+  bool cluster_ok = vec && n >= 2 && a.wait.skip_rank < 0 && env_long("RRA_RING_CLUSTER", 0) != 0;
   for (int c = 0; c < n && cluster_ok; ++c) {
     cluster_ok = (ibase[c] * e) % 16 == 0 && (obase[c] * e) % 16 == 0;
     if (c + 1 < n && len[c] % pu) cluster_ok = cluster_ok && mode == kRingAllReduce && len[c + 1] == 0;
@@ -381,6 +382,28 @@ bool all_aligned16(const void* const* p, int n) {
   return true;
 }
 
+// The measured table shipped beside the library (tune/gb300.txt next to
+// librra.so), or RRA_TUNING_FILE; loaded once, on the first rra_init.
+void load_default_tuning() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* env = std::getenv("RRA_TUNING_FILE");
+    if (env && *env) {
+      rra_load_tuning(env);
+      return;
+    }
+    Dl_info info;
+    if (!dladdr(reinterpret_cast<void*>(&rra_load_tuning), &info) || !info.dli_fname) return;
+    std::string path(info.dli_fname);
+    const size_t slash = path.rfind('/');
+    path = (slash == std::string::npos ? std::string(".") : path.substr(0, slash)) + "/tune/gb300.txt";
+    if (FILE* f = std::fopen(path.c_str(), "r")) {
+      std::fclose(f);
+      rra_load_tuning(path.c_str());
+    }
+  });
+}
+
 }  // namespace
 
 int rra::max_ctas_cap() {
@@ -437,6 +460,7 @@ rra_status_t rra_init(int device, size_t workspace_bytes) {
   s.ws.fifo = p + kFifoOffset;
   s.ws.fifo_bytes = bytes > kFifoOffset ? bytes - kFifoOffset : 0;
   s.ready = true;
+  load_default_tuning();
   return RRA_SUCCESS;
 }
 
