@@ -85,8 +85,13 @@ struct RingWarp {
     fifo_out = a.fifo + link_out * a.K * a.slot_bytes + wregion;
   }
 
+  // Flag of message m: the slot's round m / K (12 bits) under the call tag
+  // (19 bits, top bit always set, so never 0).  A slot can hold lines of
+  // any older round -- the messages between may have been empty and never
+  // written -- so the round itself must match, not just its parity; the
+  // host keeps a call under 4096 rounds per slot.
   __device__ __forceinline__ uint32_t ll_flag(uint32_t m) const {
-    return (tag << 1) + ((m / (uint32_t)a.K) & 1u) + 1u;
+    return ((((tag & 0x7FFFFu) | 0x80000u)) << 12) | ((m / (uint32_t)a.K) & 0xFFFu);
   }
 
   // Wait for the next incoming message (Simple: lane 0 acquires the head

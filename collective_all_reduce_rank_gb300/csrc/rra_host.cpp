@@ -367,6 +367,28 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
                            (long)fifo_cap, env_long("RRA_RING_CHANNELS", 16), channel_cap(n)});
   if (c < 1) return RRA_ERR_UNSUPPORTED;
+  if (proto == kProtoLL) {
+    // LL line flags carry the slot round in 12 bits: more rounds than that
+    // in one call go over the Simple protocol instead
+    const size_t iters = (maxu + (size_t)c * a.G * a.slice_units - 1) / ((size_t)c * a.G * a.slice_units);
+    const size_t sends = mode == kRingAllReduce ? 2 * (size_t)(n - 1) : (size_t)(n - 1);
+    if (iters * sends * a.G / a.K >= 4096) {
+      a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", 2L * a.G));
+      a.slot_bytes = (size_t)a.slice_units * aw * 16;
+      err = ring_occupancy(dt, vec, kProtoSimple, &occ);
+      if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
+      const size_t cap2 = s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes);
+      c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
+                          (long)cap2, env_long("RRA_RING_CHANNELS", 16), channel_cap(n)});
+      if (c < 1) return RRA_ERR_UNSUPPORTED;
+      a.channels = (int)c;
+      a.fifo = s->ws.fifo;
+      a.head = s->ws.flags;
+      a.tail = s->ws.flags + kLinkFlags;
+      *grid_out = n * (int)c;
+      return cuda_status(launch_ring(dt, vec, kProtoSimple, a, n * (int)c, st));
+    }
+  }
   a.channels = (int)c;
   a.fifo = s->ws.fifo;
   a.head = s->ws.flags;
