@@ -276,14 +276,64 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
   return cuda_status(launch_twoshot(n, dt, vec, a, n * (int)c, st));
 }
 
-// The ring's link protocol: RRA_RING_PROTO=simple|ll forces one; otherwise
-// LL up to the measured crossover (bytes per chunk), Simple above.
-int ring_proto(size_t chunk_bytes) {
+// The ring's form.  RRA_RING_PROTO=ll | simple | staged forces one (staged
+// needs 16-byte aligned buffers and chunk starts and otherwise falls back to
+// the per-warp Simple form); by default chunks up to RRA_RING_LL_MAX_BYTES
+// (64 KiB) take the per-warp LL form, larger ones the staged form.
+enum RingForm { kFormWarpSimple = 0, kFormWarpLL = 1, kFormStaged = 2 };
+
+int ring_form(size_t chunk_bytes) {
   const char* p = std::getenv("RRA_RING_PROTO");
-  if (p && !std::strcmp(p, "simple")) return kProtoSimple;
-  if (p && !std::strcmp(p, "ll")) return kProtoLL;
-  static const long limit = env_long("RRA_RING_LL_MAX_BYTES", -1);
-  return (limit < 0 || (long)chunk_bytes <= limit) ? kProtoLL : kProtoSimple;
+  if (p && !std::strcmp(p, "simple")) return kFormWarpSimple;
+  if (p && !std::strcmp(p, "ll")) return kFormWarpLL;
+  if (p && !std::strcmp(p, "staged")) return kFormStaged;
+  static const long limit = env_long("RRA_RING_LL_MAX_BYTES", 64L << 10);
+  return (long)chunk_bytes <= limit ? kFormWarpLL : kFormStaged;
+}
+
+constexpr size_t kStagedSmemBudget = 200u << 10;  // dynamic shared memory for the stages
+
+// Staged ring: messages of T units, G per step, K slots per link, D stages.
+// Defaults (measured on GB300, 8 ranks x 100 MB): T = 2048 units for 4-byte
+// types and 1024 for bfloat16 (whose partials travel as float32), G = 4,
+// K = 2G.  T shrinks (to 128 units) while the channels would outnumber the
+// tiles; K drops to G + 1 when the FIFO would not fit the workspace.
+rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t dt, cudaStream_t st,
+                             int* grid_out) {
+  const int n = a.n;
+  const size_t aw = dt == RRA_BFLOAT16 ? 2 : 1;
+  a.G = (int)std::max(1L, env_long("RRA_RING_G", 4));
+  long T = std::max(64L, std::min(4096L, env_long("RRA_RING_TILE", aw == 2 ? 1024 : 2048)));
+  auto stages_for = [&](long t) {
+    const long d = (long)(kStagedSmemBudget / ((size_t)t * 16 * (1 + aw)));
+    return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_RING_STAGES", 8)}));
+  };
+  int occ = 0;
+  cudaError_t err = ring_staged_occupancy(dt, (int)T, stages_for(T), &occ);
+  if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
+  const long cmax = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), channel_cap(n)});
+  if (cmax < 1) return RRA_ERR_UNSUPPORTED;
+  while (T > 128 && maxu < (size_t)cmax * a.G * T) T /= 2;
+  a.slice_units = (int)T;
+  a.stages = stages_for(T);
+  err = ring_staged_occupancy(dt, (int)T, a.stages, &occ);
+  if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
+  a.slot_bytes = (size_t)T * 16 * aw;
+  a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", 2L * a.G));
+  const size_t need = (maxu + (size_t)a.G * T - 1) / ((size_t)a.G * T);
+  long c = std::min<long>({cmax, (long)std::max<size_t>(1, need), env_long("RRA_RING_CHANNELS", cmax)});
+  if ((size_t)c * n * a.K * a.slot_bytes > s->ws.fifo_bytes) a.K = a.G + 1;
+  c = std::min<long>(c, (long)(s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes)));
+  if (c < 1) return RRA_ERR_UNSUPPORTED;
+  // messages per CTA stay below 2^31 (32-bit counters in the kernel)
+  const size_t iters = (maxu + (size_t)c * a.G * T - 1) / ((size_t)c * a.G * T);
+  if (iters * (size_t)(2 * n) * a.G >= (1ull << 31)) return RRA_ERR_UNSUPPORTED;
+  a.channels = (int)c;
+  a.fifo = s->ws.fifo;
+  a.head = s->ws.flags;
+  a.tail = s->ws.flags + kLinkFlags;
+  *grid_out = n * (int)c;
+  return cuda_status(launch_ring_staged(dt, a, n * (int)c, st));
 }
 
 // mode: kRingAllReduce / kRingReduceScatter / kRingAllGather.  ibase, obase,
@@ -346,8 +396,12 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
     }
     return cuda_status(err);
   }
+  const int form = ring_form(maxu * 16);
+  bool staged_ok = vec;
+  for (int c = 0; c < n; ++c) staged_ok = staged_ok && (ibase[c] * e) % 16 == 0 && (obase[c] * e) % 16 == 0;
+  if (form == kFormStaged && staged_ok) return run_ring_staged(s, a, maxu, dt, st, grid_out);
+  const int proto = form == kFormWarpLL ? kProtoLL : kProtoSimple;
   a.slice_units = kRingThreads * kRingUnitsPerThread;
-  const int proto = ring_proto(maxu * 16);
   // Credits: a rank's sends minus receives never exceed G.  Simple raises a
   // credit per message, so K > G keeps n full FIFOs from all being pending
   // at once (with K == G every rank could fill its FIFO in the first step

@@ -111,6 +111,7 @@ struct RingArgs {
   int slice_units;  // 16-byte units per message (= blockDim * units per thread)
   int G;            // messages per step and iteration
   int K;            // FIFO slots per link
+  int stages;       // staged form: shared-memory stages per CTA
   WaitCfg wait;
 };
 
@@ -182,6 +183,13 @@ int tree_tile_units_for(int dt);
 int tree_max_clusters(int n, int dt);
 cudaError_t launch_tree(int dt, const void* const* in, void* const* out, int n, size_t count, int channels, int G,
                         const WaitCfg& w, cudaStream_t s);
+
+// Ring with whole-CTA messages staged in shared memory (Simple protocol):
+// 16-byte aligned buffers and chunk starts; one link counter per (link,
+// channel); a.slice_units units per message, a.stages stages.
+size_t ring_staged_smem(int dt, int tile_units, int stages);
+cudaError_t ring_staged_occupancy(int dt, int tile_units, int stages, int* max_blocks_per_sm);
+cudaError_t launch_ring_staged(int dt, const RingArgs& a, int grid, cudaStream_t s);
 
 cudaError_t ring_occupancy(int dt, bool vec, int proto, int* max_blocks_per_sm);
 cudaError_t launch_ring(int dt, bool vec, int proto, const RingArgs& a, int grid, cudaStream_t s);

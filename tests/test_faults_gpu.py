@@ -23,7 +23,7 @@ def _init():
 
 
 @pytest.mark.parametrize("algo,proto", [(rra.RRA_ALGO_RING, "simple"), (rra.RRA_ALGO_RING, "ll"),
-                                        (rra.RRA_ALGO_TWO_SHOT, None)])
+                                        (rra.RRA_ALGO_RING, "staged"), (rra.RRA_ALGO_TWO_SHOT, None)])
 @pytest.mark.parametrize("skip", [0, 3])
 def test_crashed_rank_times_out_and_gpu_stays_usable(algo, proto, skip, monkeypatch):
     import gpu_util as g

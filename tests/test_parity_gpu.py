@@ -134,15 +134,15 @@ def test_order_sensitive_float_data(algo, dtype, n):
         _check(got[r], want[r], dtype, "%s n=%d r=%d" % (algo, n, r))
 
 
-@pytest.mark.parametrize("path", ["cluster", "simple", "ll"])
+@pytest.mark.parametrize("path", ["cluster", "simple", "ll", "staged"])
 @pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
 @pytest.mark.parametrize("n,count", [(2, 3), (3, 1001), (5, 70_001), (8, 8 * 4096 * 6 + 5), (8, 2_000_000),
                                      (4, 3 * 2048 * 8 * 4)])
 def test_ring_link_protocols(path, dtype, n, count, monkeypatch):
     # the ring on a thread-block cluster (links in distributed shared
-    # memory), or per-warp with Simple (fence + head flag) or LL (flag in
-    # every line) links in L2: same bits as the oracle's ring, for all three
-    # ring operations
+    # memory), per-warp with Simple (fence + head flag) or LL (flag in every
+    # line) links in L2, or with whole-CTA messages staged in shared memory:
+    # same bits as the oracle's ring, for all three ring operations
     if path == "cluster":
         monkeypatch.setenv("RRA_RING_CLUSTER", "1")
     else:
@@ -173,6 +173,30 @@ def test_ring_link_protocols(path, dtype, n, count, monkeypatch):
     want, _, _ = oracle.all_gather("ring", shards, dtype)
     for r in range(n):
         _check(g.to_host(outs[r], dtype), want[r], dtype, "%s ring ag r=%d" % (path, r))
+
+
+@pytest.mark.parametrize("tile,G,K,stages", [(1024, 8, 16, 8), (128, 1, 2, 1), (256, 3, 4, 2), (512, 8, 9, 3),
+                                             (4096, 2, 3, 8), (2048, 4, 8, 3)])
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n,count", [(1, 1000), (2, 3), (3, 100_003), (8, 8 * 1024 * 8 * 19 + 7), (8, 3_000_001),
+                                     (6, 4 * 4096 * 33)])
+def test_ring_staged_shapes(tile, G, K, stages, dtype, n, count, monkeypatch):
+    # the staged ring over message sizes, steps, FIFO depths and pipeline
+    # depths, including the smallest (one slot of credit beyond G, one
+    # stage) and fewer stages than slot loaders: same bits as the oracle's
+    # ring, twice in a row (the second call reuses the link counters under a
+    # new epoch), in place as well
+    monkeypatch.setenv("RRA_RING_PROTO", "staged")
+    monkeypatch.setenv("RRA_RING_CLUSTER", "0")
+    for k, v in (("RRA_RING_TILE", tile), ("RRA_RING_G", G), ("RRA_RING_K", K), ("RRA_RING_STAGES", stages)):
+        monkeypatch.setenv(k, str(v))
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=count + n + tile)
+    want, _, _ = oracle.allreduce("ring", xs, dtype)
+    for rep, inplace in enumerate((False, True)):
+        got = run_allreduce(xs, dtype, "ring", inplace=inplace)
+        for r in range(n):
+            _check(got[r], want[r], dtype, "staged n=%d r=%d rep=%d" % (n, r, rep))
 
 
 @pytest.mark.parametrize("cluster", ["0", "1"])
