@@ -21,14 +21,15 @@
 // a reader running concurrently with the writer could see a flag before
 // the rest of its line.
 //
-// Throughput: every thread (LL) or warp (LL128) keeps several line groups
-// in flight per trip of its grid-stride loop.
+// Throughput: the pack kernels give every thread (LL) or warp (LL128) one
+// group of lines over a grid that covers the payload; the unpack kernels
+// keep several groups of every source in flight per thread.  Partial groups
+// and polling take out-of-line paths, so the fast paths stay lean.
 #include "common.cuh"
 
 namespace rra {
 
-constexpr int kLLUnroll = 4;    // 16-byte payload groups per thread per trip (LL)
-constexpr int kL128Unroll = 2;  // four-line quads per warp per trip (LL128)
+constexpr int kL128Unroll = 2;  // four-line quads per warp per trip (LL128 unpack)
 
 __device__ __forceinline__ unsigned long long ll_line(uint32_t data, uint32_t flag) {
   return ((unsigned long long)flag << 32) | data;
@@ -52,6 +53,12 @@ __device__ __forceinline__ unsigned long long ld_line1(const void* p) {
   return a;
 }
 
+__device__ __forceinline__ uint2 ld_nc8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
 // payload bytes [off, off+16), zero past B
 __device__ __forceinline__ uint4 load_payload16(const unsigned char* p, size_t off, size_t B, bool vec) {
   if (vec && off + 16 <= B) return ld_stream(p + off);
@@ -62,37 +69,45 @@ __device__ __forceinline__ uint4 load_payload16(const unsigned char* p, size_t o
 
 // ---------------------------------------------------------------------------
 // LL: group g = payload bytes [16g, 16g+16) = lines 4g..4g+3 = wire bytes
-// [32g, 32g+32)
+// [32g, 32g+32).  Groups wholly inside the payload take a fast path with
+// vector accesses only; the last, partial group (and every group of an
+// unaligned payload) takes an out-of-line path, so the fast path keeps its
+// registers and no local memory.
 // ---------------------------------------------------------------------------
+static __device__ __noinline__ void ll_pack_slow(const LLArgs& a, size_t g, size_t lines) {
+  const size_t B = a.payload_bytes;
+  const uint32_t f = (uint32_t)a.flag;
+  const uint4 v = load_payload16(static_cast<const unsigned char*>(a.payload), g * 16, B, a.vec);
+  const size_t nl = lines - 4 * g < 4 ? lines - 4 * g : 4;
+  char* w = static_cast<char*>(a.wire_out) + g * 32;
+  if (nl >= 2)
+    st_lines2(w, ll_line(v.x, f), ll_line(v.y, f));
+  else
+    st_line1(w, ll_line(v.x, f));
+  if (nl == 4)
+    st_lines2(w + 16, ll_line(v.z, f), ll_line(v.w, f));
+  else if (nl == 3)
+    st_line1(w + 16, ll_line(v.z, f));
+}
+
+// One group per thread over a grid that covers the payload (the writes of a
+// CTA stay together, which the wire, twice the payload, rewards).
 __global__ void __launch_bounds__(kLLThreads) ll_pack_kernel(const __grid_constant__ LLArgs a) {
   const size_t B = a.payload_bytes;
   const size_t lines = (B + 3) / 4;
   const size_t groups = (lines + 3) / 4;
+  const size_t full = a.vec ? B / 16 : 0;  // groups with all 16 payload bytes present
   const uint32_t f = (uint32_t)a.flag;
   const unsigned char* p = static_cast<const unsigned char*>(a.payload);
   char* wire = static_cast<char*>(a.wire_out);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t g0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g0 < groups; g0 += kLLUnroll * stride) {
-    uint4 v[kLLUnroll];
-#pragma unroll
-    for (int k = 0; k < kLLUnroll; ++k) {
-      const size_t g = g0 + k * stride;
-      if (g < groups) v[k] = load_payload16(p, g * 16, B, a.vec);
-    }
-#pragma unroll
-    for (int k = 0; k < kLLUnroll; ++k) {
-      const size_t g = g0 + k * stride;
-      if (g >= groups) continue;
-      const size_t nl = lines - 4 * g < 4 ? lines - 4 * g : 4;
-      char* w = wire + g * 32;
-      if (nl >= 2)
-        st_lines2(w, ll_line(v[k].x, f), ll_line(v[k].y, f));
-      else
-        st_line1(w, ll_line(v[k].x, f));
-      if (nl == 4)
-        st_lines2(w + 16, ll_line(v[k].z, f), ll_line(v[k].w, f));
-      else if (nl == 3)
-        st_line1(w + 16, ll_line(v[k].z, f));
+  for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < groups; g += stride) {
+    if (g < full) {
+      const uint4 v = ld_stream(p + g * 16);
+      st_lines2(wire + g * 32, ll_line(v.x, f), ll_line(v.y, f));
+      st_lines2(wire + g * 32 + 16, ll_line(v.z, f), ll_line(v.w, f));
+    } else {
+      ll_pack_slow(a, g, lines);
     }
   }
 }
@@ -118,8 +133,70 @@ __device__ __forceinline__ bool ll_read4(const char* w, size_t nl, uint32_t want
   return ok;
 }
 
+// Group g whose lines are not all there yet (or the partial last group):
+// poll each source's lines, bounded, then sum in source order and store.
+// False when a wait expired or the call was aborted.
 template <int DT, int NSRC>
-__global__ void __launch_bounds__(kLLThreads) ll_unpack_kernel(const __grid_constant__ LLArgs a) {
+static __device__ __noinline__ bool ll_unpack_slow(const LLArgs& a, size_t g, size_t lines, uint32_t tag) {
+  const size_t B = a.payload_bytes;
+  const uint32_t want = (uint32_t)a.flag;
+  const size_t nl = lines - 4 * g < 4 ? lines - 4 * g : 4;
+  Acc acc;
+  for (int s = 0; s < NSRC; ++s) {
+    const char* w = static_cast<const char*>(a.wire_in[s]) + g * 32;
+    uint32_t d[4];
+    bool got = ll_read4(w, nl, want, d);
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 0; !got && it < kMaxSpin; ++it) {
+      __nanosleep(64);
+      got = ll_read4(w, nl, want, d);
+      if (got) break;
+      if ((it & 15u) == 15u) {
+        if (aborted(a.wait.status, tag)) return false;
+        if (globaltimer() - t0 > a.wait.timeout_ns) {
+          int bad = 0;  // first present line of the group whose flag differs
+          for (int i = 0; i < (int)nl; ++i)
+            if ((uint32_t)(ld_line1(w + 8 * i) >> 32) != want) {
+              bad = i;
+              break;
+            }
+          record_error(a.wait.status, RRA_ERR_TIMEOUT, s, -1, (int)(4 * g + bad), tag);
+          return false;
+        }
+      }
+    }
+    if (!got) return false;
+    const uint4 v = make_uint4(d[0], d[1], d[2], d[3]);
+    if (s == 0)
+      acc_init<DT>(acc, v);
+    else
+      acc_add<DT>(acc, v);
+  }
+  const uint4 y = acc_narrow<DT>(acc);
+  char* out = static_cast<char*>(a.out);
+  const size_t off = g * 16;
+  if (a.vec && off + 16 <= B) {
+    st_stream(out + off, y);
+  } else {
+    const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+    for (int b = 0; b < 16 && off + b < B; ++b) out[off + b] = (char)(w[b >> 2] >> (8 * (b & 3)));
+  }
+  return true;
+}
+
+// groups per thread per trip: up to 8 source-groups (256 bytes of lines)
+// in flight per thread, within the register budget of two CTAs per SM
+template <int NSRC>
+__host__ __device__ constexpr int ll_unpack_unroll() {
+  return 8 / NSRC < 1 ? 1 : (8 / NSRC > 4 ? 4 : 8 / NSRC);
+}
+
+// Grid-stride over groups on a grid the GPU holds at once (so the per-call
+// epoch costs one arrival per CTA); every line of every source of U groups
+// is loaded before any flag is tested.
+template <int DT, int NSRC>
+__global__ void __launch_bounds__(kLLThreads, 2) ll_unpack_kernel(const __grid_constant__ LLArgs a) {
+  constexpr int U = ll_unpack_unroll<NSRC>();
   __shared__ uint32_t s_epoch;
   if (threadIdx.x == 0) s_epoch = read_epoch(a.wait.sync);
   __syncthreads();
@@ -127,73 +204,49 @@ __global__ void __launch_bounds__(kLLThreads) ll_unpack_kernel(const __grid_cons
   const size_t B = a.payload_bytes;
   const size_t lines = (B + 3) / 4;
   const size_t groups = (lines + 3) / 4;
+  const size_t full = B / 16;
   const uint32_t want = (uint32_t)a.flag;
   char* out = static_cast<char*>(a.out);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  bool stop = false;
-  for (size_t g0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g0 < groups && !stop;
-       g0 += kLLUnroll * stride) {
-    uint32_t d[kLLUnroll][NSRC][4];
-    bool ok[kLLUnroll][NSRC];
-    // first pass: every line of every source in flight at once
+  for (size_t g0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g0 < groups; g0 += U * stride) {
+    unsigned long long l[U][NSRC][4];
 #pragma unroll
-    for (int k = 0; k < kLLUnroll; ++k) {
+    for (int k = 0; k < U; ++k) {
+      const size_t g = g0 + k * stride;
+      if (g < full) {
+#pragma unroll
+        for (int s = 0; s < NSRC; ++s) {
+          const char* w = static_cast<const char*>(a.wire_in[s]) + g * 32;
+          ld_lines2(w, l[k][s][0], l[k][s][1]);
+          ld_lines2(w + 16, l[k][s][2], l[k][s][3]);
+        }
+      }
+    }
+    bool stop = false;
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
       const size_t g = g0 + k * stride;
       if (g >= groups) continue;
-      const size_t nl = lines - 4 * g < 4 ? lines - 4 * g : 4;
+      bool ok = g < full && a.vec;
 #pragma unroll
       for (int s = 0; s < NSRC; ++s)
-        ok[k][s] = ll_read4(static_cast<const char*>(a.wire_in[s]) + g * 32, nl, want, d[k][s]);
-    }
 #pragma unroll
-    for (int k = 0; k < kLLUnroll; ++k) {
-      const size_t g = g0 + k * stride;
-      if (g >= groups || stop) continue;
-      const size_t nl = lines - 4 * g < 4 ? lines - 4 * g : 4;
+        for (int i = 0; i < 4; ++i) ok = ok && (uint32_t)(l[k][s][i] >> 32) == want;
+      if (ok) {
+        Acc acc;
+        acc_init<DT>(acc, make_uint4((uint32_t)l[k][0][0], (uint32_t)l[k][0][1], (uint32_t)l[k][0][2],
+                                     (uint32_t)l[k][0][3]));
 #pragma unroll
-      for (int s = 0; s < NSRC; ++s) {
-        if (ok[k][s] || stop) continue;
-        // bounded poll until the line's flags arrive
-        const char* w = static_cast<const char*>(a.wire_in[s]) + g * 32;
-        const uint64_t t0 = globaltimer();
-        bool got = false;
-        for (uint32_t it = 0; it < kMaxSpin; ++it) {
-          __nanosleep(64);
-          if (ll_read4(w, nl, want, d[k][s])) {
-            got = true;
-            break;
-          }
-          if ((it & 15u) == 15u) {
-            if (aborted(a.wait.status, tag)) break;
-            if (globaltimer() - t0 > a.wait.timeout_ns) {
-              int bad = 0;  // first present line of the group whose flag differs
-              for (int i = 0; i < (int)nl; ++i)
-                if ((uint32_t)(ld_line1(w + 8 * i) >> 32) != want) {
-                  bad = i;
-                  break;
-                }
-              record_error(a.wait.status, RRA_ERR_TIMEOUT, s, -1, (int)(4 * g + bad), tag);
-              break;
-            }
-          }
-        }
-        if (!got) stop = true;
-      }
-      if (stop) continue;
-      Acc acc;
-      acc_init<DT>(acc, make_uint4(d[k][0][0], d[k][0][1], d[k][0][2], d[k][0][3]));
-#pragma unroll
-      for (int s = 1; s < NSRC; ++s)
-        acc_add<DT>(acc, make_uint4(d[k][s][0], d[k][s][1], d[k][s][2], d[k][s][3]));
-      const uint4 y = acc_narrow<DT>(acc);
-      const size_t off = g * 16;
-      if (a.vec && off + 16 <= B) {
-        st_stream(out + off, y);
-      } else {
-        const uint32_t w[4] = {y.x, y.y, y.z, y.w};
-        for (int b = 0; b < 16 && off + b < B; ++b) out[off + b] = (char)(w[b >> 2] >> (8 * (b & 3)));
+        for (int s = 1; s < NSRC; ++s)
+          acc_add<DT>(acc, make_uint4((uint32_t)l[k][s][0], (uint32_t)l[k][s][1], (uint32_t)l[k][s][2],
+                                      (uint32_t)l[k][s][3]));
+        st_stream(out + g * 16, acc_narrow<DT>(acc));
+      } else if (!ll_unpack_slow<DT, NSRC>(a, g, lines, tag)) {
+        stop = true;
+        break;
       }
     }
+    if (stop) break;
   }
   arrive_end(a.wait.sync, epoch);
 }
@@ -203,53 +256,54 @@ __global__ void __launch_bounds__(kLLThreads) ll_unpack_kernel(const __grid_cons
 // [16(l%8), +16) of line 4q + l/8; lanes 7, 15, 23, 31 carry the line's
 // last 8 data bytes and its flag.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint2 ld_nc8(const void* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
+
+// Lane (line 4q + l/8, piece l%8) of a quad that is not complete, or of an
+// unaligned payload: byte loads, zero past the payload's end.
+static __device__ __noinline__ void ll128_pack_slow(const LLArgs& a, size_t j, int li) {
+  const size_t B = a.payload_bytes;
+  const unsigned char* p = static_cast<const unsigned char*>(a.payload);
+  const int nbytes = li < 7 ? 16 : 8;
+  const size_t off = 120 * j + 16 * li;
+  uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
+  for (int b = 0; b < nbytes && off + b < B; ++b) {
+    const uint32_t x = (uint32_t)__ldg(p + off + b) << (8 * (b & 3));
+    if (b < 4)
+      w0 |= x;
+    else if (b < 8)
+      w1 |= x;
+    else if (b < 12)
+      w2 |= x;
+    else
+      w3 |= x;
+  }
+  if (li == 7) {
+    w2 = (uint32_t)a.flag;
+    w3 = (uint32_t)(a.flag >> 32);
+  }
+  st_volatile(static_cast<char*>(a.wire_out) + 128 * j + 16 * li, make_uint4(w0, w1, w2, w3));
 }
 
+// One quad per warp over a grid that covers the payload; whole quads of an
+// aligned payload read their 120-byte line bodies with 8-byte loads (line j
+// starts at byte 120j, a multiple of 8).
 __global__ void __launch_bounds__(kLLThreads) ll128_pack_kernel(const __grid_constant__ LLArgs a) {
   const size_t B = a.payload_bytes;
   const size_t lines = (B + 119) / 120;
   const size_t quads = (lines + 3) / 4;
+  const size_t full = a.vec ? B / 480 : 0;  // quads whose four lines are complete
   const int lane = threadIdx.x & 31, li = lane & 7;
   const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
   const unsigned char* p = static_cast<const unsigned char*>(a.payload);
   char* wire = static_cast<char*>(a.wire_out);
-  const int nbytes = li < 7 ? 16 : 8;
-  for (size_t q0 = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); q0 < quads;
-       q0 += kL128Unroll * warps) {
-    uint32_t w[kL128Unroll][4];
-#pragma unroll
-    for (int k = 0; k < kL128Unroll; ++k) {
-      const size_t j = 4 * (q0 + k * warps) + (lane >> 3);
-      w[k][0] = w[k][1] = w[k][2] = w[k][3] = 0u;
-      if (j >= lines) continue;
-      const size_t off = 120 * j + 16 * li;  // 8-byte aligned
-      if (a.vec && off + nbytes <= B) {
-        const uint2 lo = ld_nc8(p + off);
-        w[k][0] = lo.x;
-        w[k][1] = lo.y;
-        if (li < 7) {
-          const uint2 hi = ld_nc8(p + off + 8);
-          w[k][2] = hi.x;
-          w[k][3] = hi.y;
-        }
-      } else {
-        for (int b = 0; b < nbytes && off + b < B; ++b)
-          w[k][b >> 2] |= (uint32_t)__ldg(p + off + b) << (8 * (b & 3));
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kL128Unroll; ++k) {
-      const size_t j = 4 * (q0 + k * warps) + (lane >> 3);
-      if (j >= lines) continue;
-      if (li == 7) {
-        w[k][2] = (uint32_t)a.flag;
-        w[k][3] = (uint32_t)(a.flag >> 32);
-      }
-      st_volatile(wire + 128 * j + 16 * li, make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]));
+  for (size_t q = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); q < quads; q += warps) {
+    const size_t j = 4 * q + (lane >> 3);
+    if (q < full) {
+      const size_t off = 120 * j + 16 * li;
+      const uint2 lo = ld_nc8(p + off);
+      const uint2 hi = li < 7 ? ld_nc8(p + off + 8) : make_uint2((uint32_t)a.flag, (uint32_t)(a.flag >> 32));
+      st_volatile(wire + 128 * j + 16 * li, make_uint4(lo.x, lo.y, hi.x, hi.y));
+    } else if (j < lines) {
+      ll128_pack_slow(a, j, li);
     }
   }
 }
@@ -357,6 +411,43 @@ cudaError_t launch_ll128_pack(const LLArgs& a, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// CTAs of `kernel` the GPU holds at once (cached per kernel)
+template <class Kern>
+static int resident_cap(Kern* kernel) {
+  static int cap = 0;  // one per instantiation of this template, i.e. per kernel
+  if (cap == 0) {
+    int dev = 0, sms = 0, occ = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kLLThreads, 0);
+    cap = (sms > 0 ? sms : 1) * (occ > 0 ? occ : 1);
+  }
+  return cap;
+}
+
+template <int DT, int NSRC>
+static cudaError_t launch_ll_unpack_n(const LLArgs& a, int grid, cudaStream_t s) {
+  auto* k = &ll_unpack_kernel<DT, NSRC>;
+  const int cap = resident_cap(k);
+  k<<<grid < cap ? grid : cap, kLLThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DT>
+static cudaError_t ll_unpack_dt(const LLArgs& a, int grid, cudaStream_t s) {
+  switch (a.nsrc) {
+    case 1: return launch_ll_unpack_n<DT, 1>(a, grid, s);
+    case 2: return launch_ll_unpack_n<DT, 2>(a, grid, s);
+    case 3: return launch_ll_unpack_n<DT, 3>(a, grid, s);
+    case 4: return launch_ll_unpack_n<DT, 4>(a, grid, s);
+    case 5: return launch_ll_unpack_n<DT, 5>(a, grid, s);
+    case 6: return launch_ll_unpack_n<DT, 6>(a, grid, s);
+    case 7: return launch_ll_unpack_n<DT, 7>(a, grid, s);
+    case 8: return launch_ll_unpack_n<DT, 8>(a, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 #define RRA_UNPACK_DISPATCH(KERNEL)                                                          \
   template <int DT>                                                                          \
   static cudaError_t KERNEL##_dt(const LLArgs& a, int grid, cudaStream_t s) {                \
@@ -374,13 +465,12 @@ cudaError_t launch_ll128_pack(const LLArgs& a, int grid, cudaStream_t s) {
     return cudaGetLastError();                                                               \
   }
 
-RRA_UNPACK_DISPATCH(ll_unpack_kernel)
 RRA_UNPACK_DISPATCH(ll128_unpack_kernel)
 
 cudaError_t launch_ll_unpack(int dt, const LLArgs& a, int grid, cudaStream_t s) {
-  if (dt == RRA_INT32) return ll_unpack_kernel_dt<RRA_INT32>(a, grid, s);
-  if (dt == RRA_FLOAT32) return ll_unpack_kernel_dt<RRA_FLOAT32>(a, grid, s);
-  return ll_unpack_kernel_dt<RRA_BFLOAT16>(a, grid, s);
+  if (dt == RRA_INT32) return ll_unpack_dt<RRA_INT32>(a, grid, s);
+  if (dt == RRA_FLOAT32) return ll_unpack_dt<RRA_FLOAT32>(a, grid, s);
+  return ll_unpack_dt<RRA_BFLOAT16>(a, grid, s);
 }
 
 cudaError_t launch_ll128_unpack(int dt, const LLArgs& a, int grid, cudaStream_t s) {

@@ -202,6 +202,13 @@ rra_status_t cuda_status(cudaError_t e) {
   return RRA_ERR_CUDA;
 }
 
+// Grid that gives every thread one unit (capped far above any real size;
+// the kernels loop past it).
+int cover_grid(size_t units, int threads) {
+  const size_t want = (units + threads - 1) / threads;
+  return (int)std::max<size_t>(1, std::min<size_t>(want, (size_t)1 << 30));
+}
+
 // Grid for a grid-stride streaming kernel: enough CTAs to give every
 // thread work, at most what the GPU holds at once.
 int stream_grid(size_t units, int threads, int per_sm) {
@@ -911,10 +918,10 @@ static rra_status_t pack_common(const char* call, bool is128, const void* payloa
   cudaError_t e;
   if (is128) {
     const size_t quads = (payload_bytes + 479) / 480;
-    grid = stream_grid(quads * 32, kLLThreads, 8);
+    grid = cover_grid(quads * 32, kLLThreads);
     e = launch_ll128_pack(a, grid, st);
   } else {
-    grid = stream_grid((payload_bytes + 15) / 16, kLLThreads, 8);
+    grid = cover_grid((payload_bytes + 15) / 16, kLLThreads);
     e = launch_ll_pack(a, grid, st);
   }
   return record(call, 0, 1, payload_bytes, -1, grid, cuda_status(e));
