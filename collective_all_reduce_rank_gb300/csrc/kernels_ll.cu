@@ -21,8 +21,8 @@
 // a reader running concurrently with the writer could see a flag before
 // the rest of its line.
 //
-// Throughput: the pack kernels give every thread (LL) or warp (LL128) one
-// group of lines over a grid that covers the payload; the unpack kernels
+// Throughput: LL pack gives every thread one group of lines over a grid that
+// covers the payload, LL128 pack one quad per warp per trip; the unpack kernels
 // keep several groups of every source in flight per thread.  Partial groups
 // and polling take out-of-line paths, so the fast paths stay lean.
 #include "common.cuh"
@@ -283,7 +283,7 @@ static __device__ __noinline__ void ll128_pack_slow(const LLArgs& a, size_t j, i
   st_volatile(static_cast<char*>(a.wire_out) + 128 * j + 16 * li, make_uint4(w0, w1, w2, w3));
 }
 
-// One quad per warp over a grid that covers the payload; whole quads of an
+// One quad per warp per trip of a grid-stride loop; whole quads of an
 // aligned payload read their 120-byte line bodies with 8-byte loads (line j
 // starts at byte 120j, a multiple of 8).
 __global__ void __launch_bounds__(kLLThreads) ll128_pack_kernel(const __grid_constant__ LLArgs a) {

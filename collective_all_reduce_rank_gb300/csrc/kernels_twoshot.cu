@@ -7,114 +7,110 @@
 // two synchronizations.
 //
 // One persistent cooperative launch of n x C CTAs.  CTA (r, ch) is channel
-// ch of virtual rank r; its 16 warps are independent pipelines.  Each
-// iteration a warp
-//   1. reduces its part of tile t of chunk r over all n inputs (ascending
-//      rank order) into outs[r], then releases its progress flag
-//      (data -> release, the Simple protocol of the same page's
-//      "Protocols" section);
-//   2. for every other rank q, acquires the flag of warp w of CTA (q, ch)
-//      for this iteration and copies that part of chunk q from outs[q] into
-//      outs[r].
-// Tile t of every chunk is handled by the same (channel, warp) in every
-// rank, so the copy reads lines a sibling CTA wrote a moment earlier and
-// finds them in L2.  No CTA-wide barrier is taken inside the loop.
+// ch of virtual rank r; its 16 warps are independent pipelines.  Warp w
+// handles tile t of every chunk in turn and, in trip i of its loop,
+//   1. issues the loads of the all-gather part of tile i - F: the other
+//      ranks' sums, from outs[q] (L2), after acquiring their progress;
+//   2. reduces tile i of chunk r over all n inputs (ascending rank order,
+//      inputs loaded one trip ahead) into outs[r];
+//   3. issues the input loads of tile i + 1;
+//   4. stores the gathered sums of tile i - F into outs[r];
+//   5. every F tiles, fences and raises its progress flag to the tiles
+//      reduced so far (data -> release, the Simple protocol of the same
+//      page's "Protocols" section).
+// The gather trails the reduce by F tiles, so the flags it needs were
+// posted F tiles earlier and it rarely waits; one fence covers F tiles; the
+// L2 loads of the gather and the HBM loads of the next inputs are in flight
+// together.  Tile t of every chunk is handled by the same (channel, warp)
+// in every rank, so the gather reads lines a sibling CTA wrote a moment
+// earlier and finds them in L2.  No CTA-wide barrier is taken in the loop.
 #include "common.cuh"
 
 namespace rra {
+
+constexpr int kTwoShotLag = 4;  // F: tiles between progress flags and of gather lag
 
 template <int N, int DT, bool VEC>
 __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch, int warp, int lane,
                                              int W, uint64_t E, uint32_t tag) {
   constexpr int PU = Elem<DT>::kPerUnit;
   constexpr int ES = Elem<DT>::kSize;
-  constexpr int UPT = kTwoShotUnitsPerThread;
+  constexpr int F = kTwoShotLag;
   const int C = a.channels;
   const size_t tile = (size_t)a.tile_units;
-  const size_t wofs = (size_t)warp * 32 * UPT;
+  const size_t wofs = (size_t)warp * 32;
   const size_t per_iter = (size_t)C * tile;
   const size_t iters = ((a.chunk_len[0] + PU - 1) / PU + per_iter - 1) / per_iter;  // chunk 0 is the longest
   uint64_t* my_flag = a.progress + ((size_t)r * C + ch) * W + warp;
   const size_t lo = a.chunk_lo[r] * ES;
   const size_t len = a.chunk_len[r];
-  // The inputs of iteration it+1 are loaded right after iteration it's
-  // reduce, so their HBM latency overlaps the all-gather part of it.
-  uint4 x[UPT][N];
-  int v[UPT];
+  auto unit_of = [&](size_t it) { return (it * C + ch) * tile + wofs + lane; };
+
+  uint4 x[N];
+  int v = 0;
   auto load_x = [&](size_t it) {
-    const size_t t0 = (it * C + ch) * tile + wofs;
+    const size_t u = unit_of(it);
+    v = unit_valid<DT>(u, len);
+    if (v > 0) {
 #pragma unroll
-    for (int j = 0; j < UPT; ++j) {
-      const size_t u = t0 + (size_t)j * 32 + lane;
-      v[j] = unit_valid<DT>(u, len);
-      if (v[j] > 0) {
-#pragma unroll
-        for (int k = 0; k < N; ++k) x[j][k] = load_in<DT, VEC>(static_cast<const char*>(a.in[k]) + lo, u, v[j]);
-      }
+      for (int k = 0; k < N; ++k) x[k] = load_in<DT, VEC>(static_cast<const char*>(a.in[k]) + lo, u, v);
     }
   };
   if (iters > 0) load_x(0);
+  uint64_t seen = 0;  // polling lane j's last observed value of peer (r + j)'s flag
 
-  for (size_t it = 0; it < iters; ++it) {
-    const size_t t0 = (it * C + ch) * tile + wofs;
-    // phase 1: reduce-scatter part
-    {
-#pragma unroll
-      for (int j = 0; j < UPT; ++j) {
-        if (v[j] > 0) {
-          Acc s;
-          acc_init<DT>(s, x[j][0]);
-#pragma unroll
-          for (int k = 1; k < N; ++k) acc_add<DT>(s, x[j][k]);
-          const size_t u = t0 + (size_t)j * 32 + lane;
-          store_out<DT, VEC, false>(static_cast<char*>(a.out[r]) + lo, u, v[j], acc_narrow<DT>(s));
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) st_release(my_flag, E | (uint64_t)(it + 1));
-    if (it + 1 < iters) load_x(it + 1);
-
-    // phase 2: all-gather part.  Lane j waits for peer (r + j) mod N, so the
-    // n-1 acquires run side by side; __syncwarp then orders every lane's
-    // reads after all of them, and the n-1 tiles are read with all loads in
-    // flight at once.
-    {
+  for (size_t it = 0; it < iters + F; ++it) {
+    // 1. gather loads of tile gi = it - F
+    const bool gather = it >= (size_t)F;
+    const size_t gi = it - F;
+    uint4 y[N > 1 ? N - 1 : 1];
+    int vy[N > 1 ? N - 1 : 1];
+    if (gather) {
       int ok = 1;
       if (lane >= 1 && lane < N) {
         const int q = (r + lane) % N;
-        if (t0 < (a.chunk_len[q] + PU - 1) / PU) {
-          uint64_t seen;
-          ok = wait_geq(a.progress + ((size_t)q * C + ch) * W + warp, E | (uint64_t)(it + 1), &seen,
-                        a.wait, tag, r, q, (int)it);
-        }
+        const uint64_t want = E | (uint64_t)(gi + 1);
+        if (unit_of(gi) - lane < (a.chunk_len[q] + PU - 1) / PU && seen < want)
+          ok = wait_geq(a.progress + ((size_t)q * C + ch) * W + warp, want, &seen, a.wait, tag, r, q, (int)gi);
       }
       ok = __all_sync(0xffffffffu, ok);
       __syncwarp();
       if (!ok) return;
-    }
-    uint4 y[N > 1 ? N - 1 : 1][UPT];
-    int v[N > 1 ? N - 1 : 1][UPT];
+      const size_t u = unit_of(gi);
 #pragma unroll
-    for (int j = 1; j < N; ++j) {
-      const int q = (r + j) % N;
-      const char* src = static_cast<const char*>(a.out[q]) + a.chunk_lo[q] * ES;
-#pragma unroll
-      for (int jj = 0; jj < UPT; ++jj) {
-        const size_t u = t0 + (size_t)jj * 32 + lane;
-        v[j - 1][jj] = unit_valid<DT>(u, a.chunk_len[q]);
-        if (v[j - 1][jj] > 0) y[j - 1][jj] = load_shared_out<DT, VEC>(src, u, v[j - 1][jj]);
+      for (int j = 1; j < N; ++j) {
+        const int q = (r + j) % N;
+        vy[j - 1] = unit_valid<DT>(u, a.chunk_len[q]);
+        if (vy[j - 1] > 0)
+          y[j - 1] = load_shared_out<DT, VEC>(static_cast<const char*>(a.out[q]) + a.chunk_lo[q] * ES, u, vy[j - 1]);
       }
     }
+    // 2-3. reduce tile it, then load the inputs of tile it + 1
+    const bool reduce = it < iters;
+    if (reduce) {
+      if (v > 0) {
+        Acc s;
+        acc_init<DT>(s, x[0]);
 #pragma unroll
-    for (int j = 1; j < N; ++j) {
-      const int q = (r + j) % N;
-      char* dst = static_cast<char*>(a.out[r]) + a.chunk_lo[q] * ES;
-#pragma unroll
-      for (int jj = 0; jj < UPT; ++jj) {
-        const size_t u = t0 + (size_t)jj * 32 + lane;
-        if (v[j - 1][jj] > 0) store_out<DT, VEC, true>(dst, u, v[j - 1][jj], y[j - 1][jj]);
+        for (int k = 1; k < N; ++k) acc_add<DT>(s, x[k]);
+        store_out<DT, VEC, false>(static_cast<char*>(a.out[r]) + lo, unit_of(it), v, acc_narrow<DT>(s));
       }
+      if (it + 1 < iters) load_x(it + 1);
+    }
+    // 4. gathered sums into this rank's output
+    if (gather) {
+      const size_t u = unit_of(gi);
+#pragma unroll
+      for (int j = 1; j < N; ++j) {
+        const int q = (r + j) % N;
+        if (vy[j - 1] > 0)
+          store_out<DT, VEC, true>(static_cast<char*>(a.out[r]) + a.chunk_lo[q] * ES, u, vy[j - 1], y[j - 1]);
+      }
+    }
+    // 5. progress: tiles 0..it reduced
+    if (reduce && ((it + 1) % F == 0 || it + 1 == iters)) {
+      __syncwarp();
+      if (lane == 0) st_release(my_flag, E | (uint64_t)(it + 1));
     }
   }
 }
