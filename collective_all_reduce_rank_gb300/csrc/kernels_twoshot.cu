@@ -7,8 +7,10 @@
 // two synchronizations.
 //
 // One persistent cooperative launch of n x C CTAs.  CTA (r, ch) is channel
-// ch of virtual rank r; its 16 warps are independent pipelines.  Warp w
-// handles tile t of every chunk in turn and, in trip i of its loop,
+// ch of virtual rank r; its 16 warps are independent pipelines, each lane
+// with 8/n (at least 1) 16-byte units per tile so that n sources keep
+// about the same bytes in flight.  Warp w handles its part of tile t of
+// every chunk in turn and, in trip i of its loop,
 //   1. issues the loads of the all-gather part of tile i - F: the other
 //      ranks' sums, from outs[q] (L2), after acquiring their progress;
 //   2. reduces tile i of chunk r over all n inputs (ascending rank order,
@@ -36,24 +38,30 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
   constexpr int PU = Elem<DT>::kPerUnit;
   constexpr int ES = Elem<DT>::kSize;
   constexpr int F = kTwoShotLag;
+  constexpr int UPT = twoshot_units_per_thread(N);  // units per lane per tile
+  constexpr int NY = N > 1 ? N - 1 : 1;
   const int C = a.channels;
-  const size_t tile = (size_t)a.tile_units;
-  const size_t wofs = (size_t)warp * 32;
+  const size_t tile = (size_t)a.tile_units;  // = threads * UPT
   const size_t per_iter = (size_t)C * tile;
   const size_t iters = ((a.chunk_len[0] + PU - 1) / PU + per_iter - 1) / per_iter;  // chunk 0 is the longest
   uint64_t* my_flag = a.progress + ((size_t)r * C + ch) * W + warp;
   const size_t lo = a.chunk_lo[r] * ES;
   const size_t len = a.chunk_len[r];
-  auto unit_of = [&](size_t it) { return (it * C + ch) * tile + wofs + lane; };
+  // first unit of this warp's part of tile `it`; lane unit j is + 32j + lane
+  auto first_of = [&](size_t it) { return (it * C + ch) * tile + (size_t)warp * 32 * UPT; };
 
-  uint4 x[N];
-  int v = 0;
+  uint4 x[UPT][N];
+  int v[UPT];
   auto load_x = [&](size_t it) {
-    const size_t u = unit_of(it);
-    v = unit_valid<DT>(u, len);
-    if (v > 0) {
+    const size_t u0 = first_of(it) + lane;
 #pragma unroll
-      for (int k = 0; k < N; ++k) x[k] = load_in<DT, VEC>(static_cast<const char*>(a.in[k]) + lo, u, v);
+    for (int j = 0; j < UPT; ++j) {
+      const size_t u = u0 + 32 * j;
+      v[j] = unit_valid<DT>(u, len);
+      if (v[j] > 0) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) x[j][k] = load_in<DT, VEC>(static_cast<const char*>(a.in[k]) + lo, u, v[j]);
+      }
     }
   };
   if (iters > 0) load_x(0);
@@ -63,48 +71,57 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
     // 1. gather loads of tile gi = it - F
     const bool gather = it >= (size_t)F;
     const size_t gi = it - F;
-    uint4 y[N > 1 ? N - 1 : 1];
-    int vy[N > 1 ? N - 1 : 1];
+    uint4 y[UPT][NY];
+    int vy[UPT][NY];
     if (gather) {
       int ok = 1;
       if (lane >= 1 && lane < N) {
         const int q = (r + lane) % N;
         const uint64_t want = E | (uint64_t)(gi + 1);
-        if (unit_of(gi) - lane < (a.chunk_len[q] + PU - 1) / PU && seen < want)
+        if (first_of(gi) < (a.chunk_len[q] + PU - 1) / PU && seen < want)
           ok = wait_geq(a.progress + ((size_t)q * C + ch) * W + warp, want, &seen, a.wait, tag, r, q, (int)gi);
       }
       ok = __all_sync(0xffffffffu, ok);
       __syncwarp();
       if (!ok) return;
-      const size_t u = unit_of(gi);
+      const size_t u0 = first_of(gi) + lane;
 #pragma unroll
-      for (int j = 1; j < N; ++j) {
-        const int q = (r + j) % N;
-        vy[j - 1] = unit_valid<DT>(u, a.chunk_len[q]);
-        if (vy[j - 1] > 0)
-          y[j - 1] = load_shared_out<DT, VEC>(static_cast<const char*>(a.out[q]) + a.chunk_lo[q] * ES, u, vy[j - 1]);
+      for (int i = 1; i < N; ++i) {
+        const int q = (r + i) % N;
+        const char* src = static_cast<const char*>(a.out[q]) + a.chunk_lo[q] * ES;
+#pragma unroll
+        for (int j = 0; j < UPT; ++j) {
+          vy[j][i - 1] = unit_valid<DT>(u0 + 32 * j, a.chunk_len[q]);
+          if (vy[j][i - 1] > 0) y[j][i - 1] = load_shared_out<DT, VEC>(src, u0 + 32 * j, vy[j][i - 1]);
+        }
       }
     }
     // 2-3. reduce tile it, then load the inputs of tile it + 1
     const bool reduce = it < iters;
     if (reduce) {
-      if (v > 0) {
-        Acc s;
-        acc_init<DT>(s, x[0]);
+      const size_t u0 = first_of(it) + lane;
 #pragma unroll
-        for (int k = 1; k < N; ++k) acc_add<DT>(s, x[k]);
-        store_out<DT, VEC, false>(static_cast<char*>(a.out[r]) + lo, unit_of(it), v, acc_narrow<DT>(s));
+      for (int j = 0; j < UPT; ++j) {
+        if (v[j] > 0) {
+          Acc s;
+          acc_init<DT>(s, x[j][0]);
+#pragma unroll
+          for (int k = 1; k < N; ++k) acc_add<DT>(s, x[j][k]);
+          store_out<DT, VEC, false>(static_cast<char*>(a.out[r]) + lo, u0 + 32 * j, v[j], acc_narrow<DT>(s));
+        }
       }
       if (it + 1 < iters) load_x(it + 1);
     }
     // 4. gathered sums into this rank's output
     if (gather) {
-      const size_t u = unit_of(gi);
+      const size_t u0 = first_of(gi) + lane;
 #pragma unroll
-      for (int j = 1; j < N; ++j) {
-        const int q = (r + j) % N;
-        if (vy[j - 1] > 0)
-          store_out<DT, VEC, true>(static_cast<char*>(a.out[r]) + a.chunk_lo[q] * ES, u, vy[j - 1], y[j - 1]);
+      for (int i = 1; i < N; ++i) {
+        const int q = (r + i) % N;
+        char* dst = static_cast<char*>(a.out[r]) + a.chunk_lo[q] * ES;
+#pragma unroll
+        for (int j = 0; j < UPT; ++j)
+          if (vy[j][i - 1] > 0) store_out<DT, VEC, true>(dst, u0 + 32 * j, vy[j][i - 1], y[j][i - 1]);
       }
     }
     // 5. progress: tiles 0..it reduced

@@ -24,7 +24,7 @@ using namespace rra;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kDefaultWorkspace = 64ull << 20;
+constexpr size_t kDefaultWorkspace = 128ull << 20;
 constexpr uint64_t kDefaultTimeoutNs = 500ull * 1000 * 1000;
 
 struct DevState {
@@ -266,7 +266,7 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
       return cuda_status(err);
     }
   }
-  a.tile_units = kDirectThreads * kTwoShotUnitsPerThread;
+  a.tile_units = kDirectThreads * twoshot_units_per_thread(n);
   int occ = 0;
   cudaError_t err = twoshot_occupancy(n, dt, vec, &occ);
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
@@ -283,58 +283,70 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
   return cuda_status(launch_twoshot(n, dt, vec, a, n * (int)c, st));
 }
 
-// The ring's form.  RRA_RING_PROTO=ll | simple | staged forces one (staged
-// needs 16-byte aligned buffers and chunk starts and otherwise falls back to
-// the per-warp Simple form); by default chunks up to RRA_RING_LL_MAX_BYTES
-// (64 KiB) take the per-warp LL form, larger ones the staged form.
+// The ring's form.  RRA_RING_PROTO=ll | simple | staged forces one.  By
+// default the staged form (measured fastest at every size on GB300: 40 us
+// against 46 us for LL at 1 KiB x 8 ranks, 78 us against 262 us at 8 MiB);
+// it needs 16-byte aligned buffers and chunk starts, and without them the
+// per-warp LL form takes chunks up to RRA_RING_LL_MAX_BYTES (64 KiB) and
+// the per-warp Simple form larger ones.
 enum RingForm { kFormWarpSimple = 0, kFormWarpLL = 1, kFormStaged = 2 };
 
-int ring_form(size_t chunk_bytes) {
+int ring_form(size_t chunk_bytes, bool staged_ok) {
   const char* p = std::getenv("RRA_RING_PROTO");
   if (p && !std::strcmp(p, "simple")) return kFormWarpSimple;
   if (p && !std::strcmp(p, "ll")) return kFormWarpLL;
-  if (p && !std::strcmp(p, "staged")) return kFormStaged;
+  if (staged_ok) return kFormStaged;
   static const long limit = env_long("RRA_RING_LL_MAX_BYTES", 64L << 10);
-  return (long)chunk_bytes <= limit ? kFormWarpLL : kFormStaged;
+  return (long)chunk_bytes <= limit ? kFormWarpLL : kFormWarpSimple;
 }
 
 constexpr size_t kStagedSmemBudget = 200u << 10;  // dynamic shared memory for the stages
 
 // Staged ring: messages of T units, G per step, K slots per link, D stages.
-// Defaults (measured on GB300, 8 ranks x 100 MB): T = 2048 units for 4-byte
-// types and 1024 for bfloat16 (whose partials travel as float32), G = 4,
-// K = 2G.  T shrinks (to 128 units) while the channels would outnumber the
-// tiles; K drops to G + 1 when the FIFO would not fit the workspace.
+// Defaults (measured on GB300, 8 ranks x 100 MB per rank): T up to 2048
+// units and G = 6 for 4-byte types, T up to 1024 and G = 8 for bfloat16
+// (whose partials travel as float32); K = 2G.  Larger G fills L2 with FIFO
+// slots (links x K x slot bytes) and runs slower.  Channels: as many as the GPU holds, but no more than
+// leave G tiles of 128 units each; then T is the smallest multiple of 32
+// units that covers the chunk in whole iterations, so no iteration runs
+// nearly empty.  K drops to G + 1 when the FIFO would not fit the workspace.
 rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t dt, cudaStream_t st,
                              int* grid_out) {
   const int n = a.n;
   const size_t aw = dt == RRA_BFLOAT16 ? 2 : 1;
-  a.G = (int)std::max(1L, env_long("RRA_RING_G", 4));
-  long T = std::max(64L, std::min(4096L, env_long("RRA_RING_TILE", aw == 2 ? 1024 : 2048)));
+  // G: the default, or fewer when the chunk fills fewer than G tiles of 128
+  // units per channel (every message of a step costs a hop, even empty)
+  const size_t gfill = (maxu + (size_t)s->sms / n * 128 - 1) / std::max<size_t>(1, (size_t)s->sms / n * 128);
+  a.G = (int)std::max(1L, env_long("RRA_RING_G", std::min<long>(aw == 2 ? 8 : 6, (long)std::max<size_t>(1, gfill))));
+  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_RING_TILE", aw == 2 ? 1024 : 2048)));
   auto stages_for = [&](long t) {
     const long d = (long)(kStagedSmemBudget / ((size_t)t * 16 * (1 + aw)));
     return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_RING_STAGES", 8)}));
   };
   int occ = 0;
-  cudaError_t err = ring_staged_occupancy(dt, (int)T, stages_for(T), &occ);
+  cudaError_t err = ring_staged_occupancy(dt, (int)tmax, stages_for(tmax), &occ);
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   const long cmax = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), channel_cap(n)});
   if (cmax < 1) return RRA_ERR_UNSUPPORTED;
-  while (T > 128 && maxu < (size_t)cmax * a.G * T) T /= 2;
+  const size_t G = (size_t)a.G;
+  long c = std::min<long>({cmax, (long)std::max<size_t>(1, (maxu + G * 128 - 1) / (G * 128)),
+                           env_long("RRA_RING_CHANNELS", cmax)});
+  c = std::max(1L, c);
+  const size_t iters = std::max<size_t>(1, (maxu + (size_t)c * G * tmax - 1) / ((size_t)c * G * tmax));
+  long T = (long)((maxu + (size_t)c * G * iters - 1) / ((size_t)c * G * iters));
+  T = std::max(32L, std::min(tmax, (T + 31) / 32 * 32));
   a.slice_units = (int)T;
   a.stages = stages_for(T);
   err = ring_staged_occupancy(dt, (int)T, a.stages, &occ);
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   a.slot_bytes = (size_t)T * 16 * aw;
   a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", 2L * a.G));
-  const size_t need = (maxu + (size_t)a.G * T - 1) / ((size_t)a.G * T);
-  long c = std::min<long>({cmax, (long)std::max<size_t>(1, need), env_long("RRA_RING_CHANNELS", cmax)});
   if ((size_t)c * n * a.K * a.slot_bytes > s->ws.fifo_bytes) a.K = a.G + 1;
   c = std::min<long>(c, (long)(s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes)));
   if (c < 1) return RRA_ERR_UNSUPPORTED;
   // messages per CTA stay below 2^31 (32-bit counters in the kernel)
-  const size_t iters = (maxu + (size_t)c * a.G * T - 1) / ((size_t)c * a.G * T);
-  if (iters * (size_t)(2 * n) * a.G >= (1ull << 31)) return RRA_ERR_UNSUPPORTED;
+  const size_t trips = (maxu + (size_t)c * a.G * T - 1) / ((size_t)c * a.G * T);
+  if (trips * (size_t)(2 * n) * a.G >= (1ull << 31)) return RRA_ERR_UNSUPPORTED;
   a.channels = (int)c;
   a.fifo = s->ws.fifo;
   a.head = s->ws.flags;
@@ -403,10 +415,10 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
     }
     return cuda_status(err);
   }
-  const int form = ring_form(maxu * 16);
   bool staged_ok = vec;
   for (int c = 0; c < n; ++c) staged_ok = staged_ok && (ibase[c] * e) % 16 == 0 && (obase[c] * e) % 16 == 0;
-  if (form == kFormStaged && staged_ok) return run_ring_staged(s, a, maxu, dt, st, grid_out);
+  const int form = ring_form(maxu * 16, staged_ok);
+  if (form == kFormStaged) return run_ring_staged(s, a, maxu, dt, st, grid_out);
   const int proto = form == kFormWarpLL ? kProtoLL : kProtoSimple;
   a.slice_units = kRingThreads * kRingUnitsPerThread;
   // Credits: a rank's sends minus receives never exceed G.  Simple raises a
@@ -415,7 +427,9 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   // and wait for a credit its successor gives only after sending too).  LL
   // raises one credit per G messages, which lags by up to G-1 more, so it
   // needs K >= 2G.
-  a.G = (int)std::max(1L, env_long("RRA_RING_G", 4));
+  // G: 4, or fewer when 16 channels of G messages would be mostly empty
+  const size_t gfill = (maxu + 16 * (size_t)a.slice_units - 1) / (16 * (size_t)a.slice_units);
+  a.G = (int)std::max(1L, env_long("RRA_RING_G", std::min<long>(4, (long)std::max<size_t>(1, gfill))));
   const long kmin = proto == kProtoLL ? 2L * a.G : (long)a.G + 1;
   a.K = (int)std::max(kmin, env_long("RRA_RING_K", 2L * a.G));
   const int aw = dt == RRA_BFLOAT16 ? 2 : 1;

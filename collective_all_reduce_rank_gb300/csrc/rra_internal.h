@@ -133,7 +133,12 @@ struct LLArgs {
 constexpr int kDirectThreads = 512;
 constexpr int kRingThreads = 512;
 constexpr int kRingUnitsPerThread = 2;
-constexpr int kTwoShotUnitsPerThread = 1;
+// Two-shot: 16-byte units per thread per tile; fewer ranks mean fewer loads
+// per unit, so more units keep the same bytes in flight.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int twoshot_units_per_thread(int n) { return n >= 5 ? 1 : (n >= 3 ? 2 : 4); }
 constexpr int kLLThreads = 256;
 
 // SM budget set by rra_set_max_ctas (0: none); kernels_direct.cu caps its

@@ -96,7 +96,7 @@ typedef enum {
 /* ------------------------------------------------------------------------ */
 
 /** Create the per-device state: the workspace (device status word, step
- *  flags, ring FIFO slots) of `workspace_bytes` bytes (0 = 64 MiB, at least
+ *  flags, ring FIFO slots) of `workspace_bytes` bytes (0 = 128 MiB, at least
  *  1 MiB) on CUDA device `device`, which becomes current.  Fixed buffers
  *  made once, ahead of the calls, keep every call allocation-free and
  *  graph-capturable, as [AIH] "Exercises" 3 explains for custom
