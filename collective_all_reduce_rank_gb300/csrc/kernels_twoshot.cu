@@ -30,14 +30,19 @@
 
 namespace rra {
 
-constexpr int kTwoShotLag = 4;  // F: tiles between progress flags and of gather lag
+// F: tiles between progress flags and of gather lag (measured on GB300: 16
+// for eight ranks, 8 for fewer)
+template <int N>
+__host__ __device__ constexpr int twoshot_lag() {
+  return N >= 8 ? 16 : 8;
+}
 
 template <int N, int DT, bool VEC>
 __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch, int warp, int lane,
                                              int W, uint64_t E, uint32_t tag) {
   constexpr int PU = Elem<DT>::kPerUnit;
   constexpr int ES = Elem<DT>::kSize;
-  constexpr int F = kTwoShotLag;
+  constexpr int F = twoshot_lag<N>();
   constexpr int UPT = twoshot_units_per_thread(N);  // units per lane per tile
   constexpr int NY = N > 1 ? N - 1 : 1;
   const int C = a.channels;
