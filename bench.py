@@ -58,6 +58,36 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def l2_copy_peak(torch):
+    """GB/s (read + write bytes) of torch's device copy between two 32 MiB
+    buffers, which stay in the 126 MB L2: the denominator for kernels whose
+    bound is L2 traffic rather than HBM (best of 20 after warm-up)."""
+    n = (32 << 20) // 4
+    a = torch.ones(n, dtype=torch.float32, device="cuda")
+    b = torch.empty_like(a)
+    for _ in range(5):
+        b.copy_(a)
+    best = None
+    for _ in range(20):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(20):
+            b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 20
+        best = ms if best is None or ms < best else best
+    return 2 * n * 4 / (best / 1e3) / 1e9
+
+
+def ring_l2_bytes(n, S):
+    """Bytes the L2-link ring moves through L2 per all-reduce of S bytes per
+    rank (4-byte types): inputs read once (n S), every one of the 2(n-1)
+    sends per rank written to a FIFO slot and read back (2 x 2(n-1) S), and
+    the outputs written once (n S)."""
+    return 2 * n * S + 4 * (n - 1) * S
+
+
 # --------------------------------------------------------------------------
 # clocks (nvidia-smi sampled during the timed region)
 # --------------------------------------------------------------------------
@@ -354,6 +384,14 @@ def run_ours(args):
     dom_name, dom_bytes = dom[0], dom[1]
     achieved = dom_bytes / (per_op[dom_name] / 1e3) / 1e9
     traffic = load_traffic(dom_name)
+    l2_peak = l2_copy_peak(torch)
+    l2_extra = None
+    if dom_name == "ar_ring":
+        l2b = ring_l2_bytes(N_RANKS, step.count * 4)
+        l2_ach = l2b / (per_op[dom_name] / 1e3) / 1e9
+        l2_extra = {"bound": "l2", "achieved": round(l2_ach, 1), "peak": round(l2_peak, 1),
+                    "peak_kind": "measured here: torch copy of an L2-resident 32 MiB buffer",
+                    "unit": "GB/s", "frac": round(l2_ach / l2_peak, 3), "l2_bytes_per_launch": l2b}
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
@@ -365,7 +403,7 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 3), "traffic": traffic},
+                     "frac": round(achieved / peak, 3), "traffic": traffic, "l2": l2_extra},
         "ops": ops,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
