@@ -295,16 +295,19 @@ __global__ void __launch_bounds__(kLLThreads) ll128_pack_kernel(const __grid_con
   const size_t warps = (size_t)gridDim.x * (blockDim.x >> 5);
   const unsigned char* p = static_cast<const unsigned char*>(a.payload);
   char* wire = static_cast<char*>(a.wire_out);
-  for (size_t q = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); q < quads; q += warps) {
+  const size_t q0 = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  // whole quads: no call in the loop
+  for (size_t q = q0; q < full; q += warps) {
     const size_t j = 4 * q + (lane >> 3);
-    if (q < full) {
-      const size_t off = 120 * j + 16 * li;
-      const uint2 lo = ld_nc8(p + off);
-      const uint2 hi = li < 7 ? ld_nc8(p + off + 8) : make_uint2((uint32_t)a.flag, (uint32_t)(a.flag >> 32));
-      st_volatile(wire + 128 * j + 16 * li, make_uint4(lo.x, lo.y, hi.x, hi.y));
-    } else if (j < lines) {
-      ll128_pack_slow(a, j, li);
-    }
+    const size_t off = 120 * j + 16 * li;
+    const uint2 lo = ld_nc8(p + off);
+    const uint2 hi = li < 7 ? ld_nc8(p + off + 8) : make_uint2((uint32_t)a.flag, (uint32_t)(a.flag >> 32));
+    st_volatile(wire + 128 * j + 16 * li, make_uint4(lo.x, lo.y, hi.x, hi.y));
+  }
+  // the rest (the payload's last, partial quad, or all of an unaligned one)
+  for (size_t q = full + (q0 + warps - full % warps) % warps; q < quads; q += warps) {
+    const size_t j = 4 * q + (lane >> 3);
+    if (j < lines) ll128_pack_slow(a, j, li);
   }
 }
 

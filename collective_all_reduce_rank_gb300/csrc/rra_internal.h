@@ -12,7 +12,7 @@
 namespace rra {
 
 constexpr int kMaxRanks = RRA_MAX_RANKS;
-constexpr int kMaxChannels = 64;  // CTAs per virtual rank in persistent kernels
+constexpr int kMaxChannels = 80;  // CTAs per virtual rank in persistent kernels (76 = 152 SMs / 2 ranks)
 
 // ---------------------------------------------------------------------------
 // workspace (one per device, made by rra_init, zero-filled)
