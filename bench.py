@@ -713,7 +713,7 @@ def run_sweep(args):
 
 def time_call(torch, call, stream, total_bytes):
     """Median microseconds per call: a CUDA graph of many calls for small
-    messages, single launches with events for large ones."""
+    messages, runs of back-to-back launches between events for large ones."""
     with torch.cuda.stream(stream):
         for _ in range(3):
             call()
@@ -734,15 +734,20 @@ def time_call(torch, call, stream, total_bytes):
             torch.cuda.synchronize()
             samples.append(a.elapsed_time(b) * 1e3 / reps)
         return statistics.median(samples)
+    # large messages: R calls back to back between two events (the host
+    # queues launches far faster than these calls run, so no launch gap is
+    # timed), median of 5 such runs
+    reps = 10 if total_bytes < (2 << 30) else 4
     samples = []
-    for _ in range(10 if total_bytes < (2 << 30) else 5):
+    for _ in range(5):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             a.record(stream)
-            call()
+            for _ in range(reps):
+                call()
             b.record(stream)
         torch.cuda.synchronize()
-        samples.append(a.elapsed_time(b) * 1e3)
+        samples.append(a.elapsed_time(b) * 1e3 / reps)
     return statistics.median(samples)
 
 
