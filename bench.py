@@ -583,6 +583,24 @@ def sample_floor(scale):
             + LL_SRC * (B + LW) + LL_SRC * LW + B + LL_SRC * (B + L8) + LL_SRC * L8 + B)
 
 
+def host_cpu():
+    """CPU model and the cores this process may run on (the oracle uses one)."""
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":")[0].strip().lower()
+            if key in ("model name", "cpu model", "hardware") and ":" in line:
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    try:
+        avail = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        avail = os.cpu_count()
+    return {"cpu_model": model, "host_cores_available": avail}
+
+
 def cpu_baseline(scale):
     import oracle
 
@@ -591,7 +609,7 @@ def cpu_baseline(scale):
     oracle_step(oracle, host, 1)
     dt = time.perf_counter() - t
     return {"value": round(sample_floor(scale) / dt / 1e9, 3), "unit": UNIT, "cores": 1,
-            "kind": "oracle", "seconds": round(dt, 2),
+            "kind": "oracle", "seconds": round(dt, 2), **host_cpu(),
             "sample": "one step at 1/%d of the workload (bucket %d elems/rank, LL payload %d B), "
                       "single-threaded C oracle" % (scale, BUCKET // scale, LL_BYTES // scale)}
 
@@ -633,7 +651,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f32,i32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "n_virtual_ranks": N_RANKS, "sample_scale": args.cpu_scale},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, **host_cpu()},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -713,10 +731,11 @@ def run_sweep(args):
                 best = None
                 for name, algo in algos:
                     call = lambda: rra.rra_allreduce(ins, outs, count, code, rra.RRA_SUM, algo, stream)
-                    us = time_call(torch, call, stream, S * n)
+                    us, p10, p90 = time_call(torch, call, stream, S * n)
                     fb = 2 * n * S
                     alg = S / (us / 1e6) / 1e9
                     row = {"n": n, "dtype": dtype, "bytes_per_rank": S, "algo": name, "us": round(us, 3),
+                           "us_p10": round(p10, 3), "us_p90": round(p90, 3),
                            "algbw": round(alg, 2), "busbw": round(alg * 2 * (n - 1) / n, 2),
                            "floor_bytes": fb, "GBps": round(fb / (us / 1e6) / 1e9, 1),
                            "pct_hbm_8TBps": round(100 * fb / (us / 1e6) / 1e9 / HBM_NOMINAL, 1),
@@ -734,6 +753,13 @@ def run_sweep(args):
         f.write("# nranks dtype log2_bytes algo  (fastest measured schedule per size)\n")
         for n, dtype, lb, name in tune:
             f.write("%d %s %d %s\n" % (n, dtype, lb, name))
+
+
+def spread(samples):
+    """(median, p10, p90) of a list of timings."""
+    q = sorted(samples)
+    pick = lambda f: q[min(len(q) - 1, max(0, int(round(f * (len(q) - 1)))))]
+    return statistics.median(q), pick(0.1), pick(0.9)
 
 
 def time_call(torch, call, stream, total_bytes):
@@ -758,7 +784,7 @@ def time_call(torch, call, stream, total_bytes):
             b.record(stream)
             torch.cuda.synchronize()
             samples.append(a.elapsed_time(b) * 1e3 / reps)
-        return statistics.median(samples)
+        return spread(samples)
     # large messages: R calls back to back between two events (the host
     # queues launches far faster than these calls run, so no launch gap is
     # timed), median of 5 such runs
@@ -773,7 +799,7 @@ def time_call(torch, call, stream, total_bytes):
             b.record(stream)
         torch.cuda.synchronize()
         samples.append(a.elapsed_time(b) * 1e3 / reps)
-    return statistics.median(samples)
+    return spread(samples)
 
 
 def run_profile(args):
