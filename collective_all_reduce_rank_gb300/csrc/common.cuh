@@ -302,10 +302,13 @@ __device__ __forceinline__ bool aborted(const DevStatus* st, uint32_t tag) {
 // Wait until *flag >= target; *seen gets the value observed.  Returns false
 // (after recording a timeout unless another wait already gave up) when the
 // wait expires or the call was aborted.  Never unbounded: a %globaltimer
-// limit plus an iteration cap.
+// limit plus an iteration cap.  An expired wait is the "root" record when
+// the peer never joined the call: by default when the awaited flag itself
+// holds an earlier call's value; with `joined`, when the peer's joined flag
+// (raised by each of its CTAs before any wait) does.
 static __device__ __noinline__ bool wait_geq(const uint64_t* flag, uint64_t target, uint64_t* seen,
                                       const WaitCfg& w, uint32_t tag, int rank, int peer,
-                                      int index) {
+                                      int index, const uint64_t* joined = nullptr) {
   uint64_t v = ld_acquire(flag);
   if (v >= target) {
     *seen = v;
@@ -324,9 +327,9 @@ static __device__ __noinline__ bool wait_geq(const uint64_t* flag, uint64_t targ
     }
     __nanosleep(64);
   }
-  // The flag still holds a value of an earlier call: the peer posted nothing
-  // in this one.
-  const bool root = (v >> 32) != (target >> 32);
+  // The flag (or the peer's joined flag) still holds a value of an earlier
+  // call: the peer took no part in this one.
+  const bool root = joined ? (ld_acquire(joined) >> 32) != (target >> 32) : (v >> 32) != (target >> 32);
   record_error(w.status, RRA_ERR_TIMEOUT, rank, peer, index, tag, root);
   return false;
 }

@@ -355,6 +355,63 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
   return cuda_status(launch_ring_staged(dt, a, n * (int)c, st));
 }
 
+// Staged tree: one message per tile of T units (T <= RRA_TREE_TILE: 1024 for
+// 4-byte types, 512 for bfloat16, whose partials travel as float32), G tiles
+// per iteration (RRA_TREE_G, 24), K = G + 1 FIFO slots per link
+// (RRA_TREE_K), stages as shared memory allows; T balanced over whole
+// iterations as in the staged ring.  Measured on GB300 at 8 x 100 MB: G
+// hides the up-and-back wave of each iteration (G = 4: 0.86 TB/s, 16: 1.58,
+// 24: 1.77, 32: 1.56, when the FIFO crowds L2).
+rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* out, int n, size_t count,
+                             rra_dtype_t dt, cudaStream_t st, int* grid_out) {
+  StagedTreeArgs a{};
+  const size_t e = elem_size(dt), aw = dt == RRA_BFLOAT16 ? 2 : 1;
+  for (int r = 0; r < n; ++r) {
+    a.in[r] = in[r];
+    a.out[r] = out[r];
+  }
+  a.n = n;
+  a.count = count;
+  const size_t units = (count * e + 15) / 16;
+  a.G = (int)std::max(1L, env_long("RRA_TREE_G", 24));
+  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_TREE_TILE", aw == 2 ? 512 : 1024)));
+  auto stages_for = [&](long t) {
+    const long d = (long)(kStagedSmemBudget / ((size_t)t * 16 * (1 + 2 * aw)));
+    return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_TREE_STAGES", 8)}));
+  };
+  int occ = 0;
+  cudaError_t err = tree_staged_occupancy(dt, (int)tmax, stages_for(tmax), &occ);
+  if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
+  const long cmax = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), channel_cap(n)});
+  if (cmax < 1) return RRA_ERR_UNSUPPORTED;
+  const size_t G = (size_t)a.G;
+  long c = std::min<long>({cmax, (long)std::max<size_t>(1, (units + G * 128 - 1) / (G * 128)),
+                           env_long("RRA_TREE_CHANNELS", cmax)});
+  c = std::max(1L, c);
+  const size_t iters = std::max<size_t>(1, (units + (size_t)c * G * tmax - 1) / ((size_t)c * G * tmax));
+  long T = (long)((units + (size_t)c * G * iters - 1) / ((size_t)c * G * iters));
+  T = std::max(32L, std::min(tmax, (T + 31) / 32 * 32));
+  a.slice_units = (int)T;
+  a.stages = stages_for(T);
+  err = tree_staged_occupancy(dt, (int)T, a.stages, &occ);
+  if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
+  a.slot_bytes = (size_t)T * 16 * aw;
+  a.K = (int)std::max((long)a.G + 1, env_long("RRA_TREE_K", (long)a.G + 1));
+  if ((size_t)c * 2 * n * a.K * a.slot_bytes > s->ws.fifo_bytes) a.K = a.G + 1;
+  c = std::min<long>(c, (long)(s->ws.fifo_bytes / ((size_t)2 * n * a.K * a.slot_bytes)));
+  if (c < 1 || (size_t)3 * n * c > kLinkFlags) return RRA_ERR_UNSUPPORTED;
+  const size_t trips = (units + (size_t)c * a.G * T - 1) / ((size_t)c * a.G * T);
+  if (trips * 2 * (size_t)a.G >= (1ull << 31)) return RRA_ERR_UNSUPPORTED;
+  a.channels = (int)c;
+  a.fifo = s->ws.fifo;
+  a.head = s->ws.flags;
+  a.tail = s->ws.flags + kLinkFlags;
+  a.joined = s->ws.flags + 2 * kLinkFlags;  // the two-shot progress words, unused by a tree call
+  a.wait = wait_cfg(s);
+  *grid_out = n * (int)c;
+  return cuda_status(launch_tree_staged(dt, a, n * (int)c, st));
+}
+
 // mode: kRingAllReduce / kRingReduceScatter / kRingAllGather.  ibase, obase,
 // len: per chunk, in elements.
 rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int n, int mode,
@@ -721,7 +778,9 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
   if (!s || !s->ready) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_NOT_INITIALIZED);
   int grid = 0;
   rra_status_t rs;
-  if (algo == RRA_ALGO_TREE) {
+  if (algo == RRA_ALGO_TREE && env_long("RRA_TREE_CLUSTER", 0) == 0) {
+    rs = run_tree_staged(s, bufs, outs, nranks, count, dtype, st, &grid);
+  } else if (algo == RRA_ALGO_TREE) {
     const int maxc = tree_max_clusters(nranks, dtype);
     if (maxc <= 0) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_UNSUPPORTED);
     const int G = (int)std::max(1L, std::min(4L, env_long("RRA_TREE_G", 2)));

@@ -115,6 +115,28 @@ struct RingArgs {
   WaitCfg wait;
 };
 
+// Staged tree all-reduce (persistent, cooperative).  Per channel: up FIFO
+// of node r at link r, down FIFO at link n + r; heads [2n x channels]
+// (up, then down); tails [3n x channels] (up; down read by the left child;
+// down read by the right child).
+struct StagedTreeArgs {
+  const void* in[kMaxRanks];
+  void* out[kMaxRanks];
+  size_t count;  // elements per rank
+  char* fifo;    // 2n links x channels x K slots x slot_bytes
+  uint64_t* head;
+  uint64_t* tail;
+  uint64_t* joined;  // [n x channels]: the call's epoch once the CTA has started
+  size_t slot_bytes;
+  int n;
+  int channels;
+  int slice_units;  // 16-byte units per message
+  int G;            // tiles per iteration
+  int K;            // FIFO slots per link
+  int stages;       // shared-memory stages per CTA
+  WaitCfg wait;
+};
+
 struct LLArgs {
   const void* wire_in[kMaxRanks];
   void* out;
@@ -195,6 +217,11 @@ cudaError_t launch_tree(int dt, const void* const* in, void* const* out, int n, 
 size_t ring_staged_smem(int dt, int tile_units, int stages);
 cudaError_t ring_staged_occupancy(int dt, int tile_units, int stages, int* max_blocks_per_sm);
 cudaError_t launch_ring_staged(int dt, const RingArgs& a, int grid, cudaStream_t s);
+
+// Staged tree: 16-byte aligned buffers.
+size_t tree_staged_smem(int dt, int tile_units, int stages);
+cudaError_t tree_staged_occupancy(int dt, int tile_units, int stages, int* max_blocks_per_sm);
+cudaError_t launch_tree_staged(int dt, const StagedTreeArgs& a, int grid, cudaStream_t s);
 
 cudaError_t ring_occupancy(int dt, bool vec, int proto, int* max_blocks_per_sm);
 cudaError_t launch_ring(int dt, bool vec, int proto, const RingArgs& a, int grid, cudaStream_t s);

@@ -23,7 +23,8 @@ def _init():
 
 
 @pytest.mark.parametrize("algo,proto", [(rra.RRA_ALGO_RING, "simple"), (rra.RRA_ALGO_RING, "ll"),
-                                        (rra.RRA_ALGO_RING, "staged"), (rra.RRA_ALGO_TWO_SHOT, None)])
+                                        (rra.RRA_ALGO_RING, "staged"), (rra.RRA_ALGO_TWO_SHOT, None),
+                                        (rra.RRA_ALGO_TREE, None)])
 @pytest.mark.parametrize("skip", [0, 3])
 def test_crashed_rank_times_out_and_gpu_stays_usable(algo, proto, skip, monkeypatch):
     import gpu_util as g
@@ -49,7 +50,7 @@ def test_crashed_rank_times_out_and_gpu_stays_usable(algo, proto, skip, monkeypa
     rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, algo)
     st, info = rra.rra_query_status()
     assert st == 0, info
-    name = "ring" if algo == rra.RRA_ALGO_RING else "twoshot"
+    name = {rra.RRA_ALGO_RING: "ring", rra.RRA_ALGO_TREE: "tree"}.get(algo, "twoshot")
     want, _, _ = oracle.allreduce(name, xs, "float32")
     for r in range(n):
         g.assert_bits_equal(g.to_host(outs[r], "float32"), want[r], "after recovery")

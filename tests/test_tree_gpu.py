@@ -41,6 +41,48 @@ def test_tree_matches_oracle(dtype, n, count):
             g.assert_bits_equal(got, want[r], "tree n=%d r=%d inplace=%s" % (n, r, inplace))
 
 
+@pytest.mark.parametrize("tile,G,K,stages", [(1024, 4, 8, 8), (128, 1, 2, 1), (256, 3, 4, 2), (512, 8, 9, 3),
+                                             (2048, 2, 3, 8)])
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n,count", [(2, 3), (3, 100_003), (5, 70_001), (8, 8 * 1024 * 4 * 19 + 7), (8, 3_000_001)])
+def test_staged_tree_shapes(tile, G, K, stages, dtype, n, count, monkeypatch):
+    # the staged tree over message sizes, tiles per iteration, FIFO depths
+    # and pipeline depths, down to one slot of credit beyond G and one stage:
+    # the oracle's tree bits, twice in a row and in place
+    import gpu_util as g
+
+    for k, v in (("RRA_TREE_TILE", tile), ("RRA_TREE_G", G), ("RRA_TREE_K", K), ("RRA_TREE_STAGES", stages)):
+        monkeypatch.setenv(k, str(v))
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=count + n + tile)
+    want, _, _ = oracle.allreduce("tree", xs, dtype)
+    for inplace in (False, True):
+        ins = [g.to_dev(x, dtype) for x in xs]
+        outs = ins if inplace else g.empty(n, count, dtype)
+        rra.rra_allreduce(ins, outs, count, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_TREE)
+        st, info = rra.rra_query_status()
+        assert st == 0, info
+        for r in range(n):
+            g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "staged tree n=%d r=%d" % (n, r))
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("n,count", [(3, 100_003), (8, 3_000_001)])
+def test_cluster_tree_form(dtype, n, count, monkeypatch):
+    # the tree on thread-block clusters (links in distributed shared memory)
+    import gpu_util as g
+
+    monkeypatch.setenv("RRA_TREE_CLUSTER", "1")
+    xs = inputs.make_ranks(n, count, dtype, "normal", seed=count)
+    want, _, _ = oracle.allreduce("tree", xs, dtype)
+    ins = [g.to_dev(x, dtype) for x in xs]
+    outs = g.empty(n, count, dtype)
+    rra.rra_allreduce(ins, outs, count, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_TREE)
+    assert rra.rra_query_status()[0] == 0
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "cluster tree n=%d r=%d" % (n, r))
+
+
 def test_tree_order_case_on_gpu():
     # the hand-derived n = 4 case of the oracle's pins: (0, 1.5) per column
     import gpu_util as g
