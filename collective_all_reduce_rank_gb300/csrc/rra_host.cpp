@@ -778,7 +778,9 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
   if (!s || !s->ready) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_NOT_INITIALIZED);
   int grid = 0;
   rra_status_t rs;
-  if (algo == RRA_ALGO_TREE && env_long("RRA_TREE_CLUSTER", 0) == 0) {
+  // the cluster form only without fault injection: a silent rank would
+  // leave its cluster peers at a hardware barrier
+  if (algo == RRA_ALGO_TREE && (env_long("RRA_TREE_CLUSTER", 0) == 0 || g_skip_rank.load() >= 0)) {
     rs = run_tree_staged(s, bufs, outs, nranks, count, dtype, st, &grid);
   } else if (algo == RRA_ALGO_TREE) {
     const int maxc = tree_max_clusters(nranks, dtype);

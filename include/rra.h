@@ -87,7 +87,9 @@ typedef enum {
   /** all-reduce only: reduce up a binary tree, broadcast down it ([AIH]
    *  "Algorithms": tree, O(log n) steps).  Heap order (parent of r is
    *  (r-1)/2); node r sums its own data, then its left child's partial,
-   *  then its right child's.  Needs 16-byte aligned buffers. */
+   *  then its right child's; the root's total, rounded once, travels down
+   *  unchanged.  Needs 16-byte aligned buffers.  Links through the
+   *  workspace (RRA_TREE_CLUSTER=1: through thread-block clusters). */
   RRA_ALGO_TREE = 6
 } rra_algo_t;
 
@@ -301,8 +303,9 @@ void rra_set_timeout_ns(uint64_t ns);
 void rra_set_max_ctas(int max_ctas);
 
 /** Fault injection for tests: virtual rank `rank` posts no step flag in the
- *  following ring and two-shot calls (-1 turns it off), so its peers' waits
- *  expire with RRA_ERR_TIMEOUT naming it as `peer`.  The GPU stays usable. */
+ *  following ring, two-shot and tree calls (-1 turns it off), so its peers'
+ *  waits expire with RRA_ERR_TIMEOUT naming it as `peer`.  The GPU stays
+ *  usable. */
 void rra_debug_skip_rank(int rank);
 
 /** Static text for a status code. */
