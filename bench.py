@@ -225,6 +225,8 @@ class Step:
             rra.rra_allreduce(self.x, self.ar_out, self.count, F, SUM, rra.RRA_ALGO_ONE_SHOT, stream)
         elif name == "ar_twoshot":
             rra.rra_allreduce(self.x, self.ar_out, self.count, F, SUM, rra.RRA_ALGO_TWO_SHOT, stream)
+        elif name == "ar_tree":  # a row beyond the step (profiling only)
+            rra.rra_allreduce(self.x, self.ar_out, self.count, F, SUM, rra.RRA_ALGO_TREE, stream)
         elif name == "rs_ring":
             rra.rra_reduce_scatter(self.x, self.rs_out, self.rc, F, SUM, rra.RRA_ALGO_RING, stream)
         elif name == "rs_direct":
