@@ -180,7 +180,6 @@ __global__ void __launch_bounds__(kCRingThreads, 1) ring_cluster_kernel(const __
       const bool uses_x = mode == kRingAllGather ? k == 0 : k <= n - 1;
       const bool final_rs = mode != kRingAllGather && k == n - 1;
       const bool ag_store = mode == kRingAllGather ? true : (mode == kRingAllReduce && k >= n);
-      const bool partial_in = recv && mode != kRingAllGather && k <= n - 1;
       const bool partial_out = send && mode != kRingAllGather && k <= n - 2;
       // chunk this action stores / reduces
       const int c = mode == kRingAllGather ? ((r - k) % n + n) % n
