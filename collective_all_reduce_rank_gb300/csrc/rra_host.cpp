@@ -651,16 +651,14 @@ rra_algo_t rra_select_algo(int nranks, size_t bytes_per_rank, rra_dtype_t dtype)
       }
     if (best_a >= 0) return (rra_algo_t)best_a;
   }
-  // Prior: the alpha-beta model of the "Algorithms" section with one-GPU
-  // constants.  Every virtual rank's traffic crosses the same HBM, so beta
-  // is the HBM bandwidth; alpha is one flag round trip through L2.  One-shot
-  // (2 alpha + (n-1) S / beta) against two-shot (4 alpha + 2 (n-1)/n S /
-  // beta): one-shot up to S* = 2 alpha beta / ((n-1)(1-2/n)).
-  const double alpha = 2.0e-6, beta = 6.5e12;
-  const double den = (nranks - 1) * (1.0 - 2.0 / nranks);
-  if (den <= 0) return RRA_ALGO_ONE_SHOT;
-  const double s_star = 2 * alpha * beta / den;
-  return (double)bytes_per_rank <= s_star ? RRA_ALGO_ONE_SHOT : RRA_ALGO_TWO_SHOT;
+  // Prior: the alpha-beta model of the "Algorithms" section, with the
+  // traffic of one GPU.  There, the n ranks' peer reads of a unit are the
+  // same HBM bytes, so one-shot moves 2nS (every input read once, every
+  // output written once) -- the same beta term as two-shot and the ring --
+  // with one synchronization against two-shot's two and the ring's 2(n-1):
+  // one-shot at every size (the measured table agrees at every size swept).
+  (void)dtype;
+  return RRA_ALGO_ONE_SHOT;
 }
 
 rra_status_t rra_load_tuning(const char* path) {

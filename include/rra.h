@@ -276,10 +276,13 @@ rra_status_t rra_ll128_unpack(const void* const* wires, int nsrc, void* out, siz
 rra_status_t rra_query_status(rra_stream_t stream, int32_t info[4]);
 
 /** The schedule AUTO uses for an all-reduce of bytes_per_rank bytes per
- *  rank: from the measured table (rra_load_tuning) when one is loaded,
- *  else from the alpha-beta cost model of [AIH] "Algorithms" with this
- *  GPU's constants (one-shot up to the model's crossover, [AIH]
- *  "Exercises" 2, two-shot above it).  Never returns RRA_ALGO_AUTO. */
+ *  rank: from the measured table (rra_load_tuning; the table shipped
+ *  beside the library is loaded by rra_init) when it has an entry for
+ *  nranks and dtype, else from the alpha-beta cost model of [AIH]
+ *  "Algorithms" with the traffic of one GPU, where the ranks' peer reads
+ *  are the same HBM bytes: every schedule then moves the same 2nS bytes
+ *  and one-shot has the fewest synchronizations, so the model gives
+ *  one-shot at every size.  Never returns RRA_ALGO_AUTO. */
 rra_algo_t rra_select_algo(int nranks, size_t bytes_per_rank, rra_dtype_t dtype);
 
 /** Load a tuning table: text lines "nranks dtype log2_bytes algo" (dtype
