@@ -587,15 +587,18 @@ def sample_floor(scale):
 
 def host_cpu():
     """CPU model and the cores this process may run on (the oracle uses one)."""
-    model = None
+    model, arm = None, {}
     try:
         for line in open("/proc/cpuinfo"):
             key = line.split(":")[0].strip().lower()
-            if key in ("model name", "cpu model", "hardware") and ":" in line:
+            if key in ("model name", "cpu model", "hardware") and ":" in line and model is None:
                 model = line.split(":", 1)[1].strip()
-                break
+            elif key in ("cpu implementer", "cpu part") and ":" in line:
+                arm.setdefault(key, line.split(":", 1)[1].strip())
     except OSError:
         pass
+    if model is None and arm:  # Arm cores list implementer and part codes only
+        model = "arm implementer %s part %s" % (arm.get("cpu implementer"), arm.get("cpu part"))
     try:
         avail = len(os.sched_getaffinity(0))
     except (AttributeError, OSError):
