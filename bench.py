@@ -90,10 +90,11 @@ def l2_copy_peak(torch):
 
 def ring_l2_bytes(n, S):
     """Bytes the L2-link ring moves through L2 per all-reduce of S bytes per
-    rank (4-byte types): inputs read once (n S), every one of the 2(n-1)
-    sends per rank written to a FIFO slot and read back (2 x 2(n-1) S), and
-    the outputs written once (n S)."""
-    return 2 * n * S + 4 * (n - 1) * S
+    rank (4-byte types): inputs read once (n S), outputs written once (n S),
+    each of the n-1 reduce-scatter partials per rank written to a FIFO slot
+    and read back (2 (n-1) S over all ranks), and each of the n-1 forwarded
+    values per rank read from the sender's output ((n-1) S)."""
+    return 2 * n * S + 3 * (n - 1) * S
 
 
 # --------------------------------------------------------------------------

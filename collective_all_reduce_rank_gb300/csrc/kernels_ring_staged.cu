@@ -20,19 +20,25 @@
 //     into stage q mod D (it never waits on a peer, so HBM reads run ahead);
 //   warps 1..P (P loaders, message q taken by warp 1 + q mod P): acquire
 //     the incoming head counter and the outgoing tail counter side by side,
-//     then bulk-copy the incoming slot into the stage.  Each acquire is an
+//     then bulk-copy the incoming message into the stage.  Each acquire is an
 //     L2 round trip; P warps keep P of them in flight.  At most D of them
 //     work: a loader tests the "stage free" mbarrier by phase parity, which
 //     is only sound while it cannot be 2D messages ahead of the consumers,
 //     and a loader's previous message (P earlier) bounds that lead to
 //     P + D <= 2D;
 //   warps P+2.. (consumers): wait for both copies, add, write the outgoing
-//     slot and / or the output, release the stage, publish "message q done";
+//     slot or the output, release the stage, publish "message q done";
 //   warp P+1 (signaller): once every consumer warp has finished a run of
 //     messages, one fence then one head update for all of them, so the
 //     fence latency is paid once per batch and never stalls a consumer.
 // Each step sends G messages, so the message a rank needs next was posted G
-// messages earlier and the hop latency hides behind the other G-1.  Only
+// messages earlier and the hop latency hides behind the other G-1.
+// Reduce-scatter partials travel through the FIFO slots; a value already in
+// the element type (the finished chunk, and every all-gather forward) is
+// not copied into a slot: the sender stores it in its own output, kept in
+// L2, and posts it, and the receiver bulk-copies it from there (an output is
+// never rewritten within a call, so these messages need no credit).  That
+// halves the slot writes, and L2 bandwidth is what bounds this ring.  Only
 // the inputs are read from HBM and only the outputs written to it.  Every
 // role walks the message sequence with counters (no integer division on
 // the per-message path), and every mbarrier wait suspends the warp in
@@ -71,8 +77,8 @@ struct StagedCursor {
 struct StagedMsg {
   int c;           // chunk
   bool x;          // reads the rank's own input tile
-  bool in;         // receives a message
-  bool send;       // sends a message
+  bool in;         // receives a message (pulled from the sender's output when !x)
+  bool send;       // sends a message (posted in its own output when store)
   bool store;      // writes the output
   int nw;          // 16-byte words per unit in the incoming message
   size_t base;     // first unit of the tile inside chunk c
@@ -187,9 +193,9 @@ __device__ __forceinline__ void staged_partial(const unsigned char* xs, const un
 }
 
 // last reduce-scatter step (or the all-gather's own shard): the value in
-// the element type -> output, and -> outgoing slot when sending
+// the element type -> output (posted to the successor when sending)
 template <int DT>
-__device__ __forceinline__ void staged_final(const unsigned char* xs, const unsigned char* ps, char* so, char* yg,
+__device__ __forceinline__ void staged_final(const unsigned char* xs, const unsigned char* ps, char* yg,
                                              size_t base, uint32_t u0, uint32_t units, bool in, bool send) {
   constexpr int AW = Elem<DT>::kAccWords;
   constexpr int B = staged_batch<DT>();
@@ -217,15 +223,19 @@ __device__ __forceinline__ void staged_final(const unsigned char* xs, const unsi
         acc_init<DT>(s, xv[k]);
       }
       const uint4 val = acc_narrow<DT>(s);
-      st_stream(yg + (base + u) * 16, val);
-      if (send) st_l2(so + (size_t)u * 16, val);
+      // a posted value stays in L2 for the successor's read
+      if (send)
+        st_l2(yg + (base + u) * 16, val);
+      else
+        st_stream(yg + (base + u) * 16, val);
     }
   }
 }
 
-// all-gather step: incoming value -> output, and forwarded when sending
+// all-gather step: incoming value -> output (posted to the successor when
+// sending)
 template <int DT>
-__device__ __forceinline__ void staged_forward(const unsigned char* ps, char* so, char* yg, size_t base, uint32_t u0,
+__device__ __forceinline__ void staged_forward(const unsigned char* ps, char* yg, size_t base, uint32_t u0,
                                                uint32_t units, bool send) {
   constexpr int B = staged_batch<DT>();
   uint4 v[B];
@@ -238,8 +248,10 @@ __device__ __forceinline__ void staged_forward(const unsigned char* ps, char* so
   for (int k = 0; k < B; ++k) {
     const uint32_t u = u0 + k * kStagedNT;
     if (u < units) {
-      st_stream(yg + (base + u) * 16, v[k]);
-      if (send) st_l2(so + (size_t)u * 16, v[k]);
+      if (send)
+        st_l2(yg + (base + u) * 16, v[k]);
+      else
+        st_stream(yg + (base + u) * 16, v[k]);
     }
   }
 }
@@ -248,16 +260,20 @@ __device__ __forceinline__ void staged_forward(const unsigned char* ps, char* so
 // thread at a time, element-wise where the unit is partial.
 template <int DT>
 __device__ __forceinline__ void staged_ragged(const StagedMsg& m, const unsigned char* xs, const unsigned char* ps,
-                                              char* so, const char* xg, char* yg, size_t len, int tid) {
+                                              char* so, const char* xg, const char* pg, char* yg, size_t len,
+                                              int tid) {
   constexpr int AW = Elem<DT>::kAccWords;
   for (uint32_t u = tid; u < m.units; u += kStagedNT) {
     const size_t gu = m.base + u;
     const int v = unit_valid<DT>(gu, len);
     if (!m.x) {
-      // all-gather step: the value arrives in the element type
-      const uint4 val = lds128(ps + (size_t)u * 16);
-      store_out<DT, true, true>(yg, gu, v, val);
-      if (m.send) st_l2(so + (size_t)u * 16, val);
+      // all-gather step: the value, in the element type, from the sender's
+      // output (its partial last unit read directly)
+      const uint4 val = u < m.xfull ? lds128(ps + (size_t)u * 16) : ld_partial_l2<DT>(pg + gu * 16, v);
+      if (m.send)
+        store_out<DT, true, false>(yg, gu, v, val);
+      else
+        store_out<DT, true, true>(yg, gu, v, val);
       continue;
     }
     const uint4 xv = u < m.xfull ? lds128(xs + (size_t)u * 16) : ld_partial<DT>(xg + gu * 16, v);
@@ -278,8 +294,10 @@ __device__ __forceinline__ void staged_ragged(const StagedMsg& m, const unsigned
       if (AW == 2) st_l2(so + (size_t)u * 16 * AW + 16, o[1]);
     } else {
       const uint4 val = acc_narrow<DT>(s);
-      store_out<DT, true, true>(yg, gu, v, val);
-      if (m.send) st_l2(so + (size_t)u * 16, val);
+      if (m.send)
+        store_out<DT, true, false>(yg, gu, v, val);
+      else
+        store_out<DT, true, true>(yg, gu, v, val);
     }
   }
 }
@@ -345,18 +363,22 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
     uint64_t* full = px ? sh.fullx : sh.fullp;
     StagedCursor k;
     StagedStage st;
-    uint32_t m_in = 0, m_out = 0, slot_in = 0;
+    // m_in: messages received (head counter); s_in / s_out: partials
+    // received / sent through slots (slot index, credits)
+    uint32_t m_in = 0, s_in = 0, s_out = 0, slot_in = 0;
     uint64_t seen_head = 0, seen_tail = 0;
     uint32_t q = 0;
     if (mine >= np) q = Q;  // idle P loader
     for (; q < Q; ++q, k.next(G, steps), st.next(D), pos = pos + 1 == np ? 0u : pos + 1) {
       const StagedMsg m = staged_msg<DT>(a, r, ch, k);
+      const bool slot_recv = m.in && m.x, slot_send = m.send && !m.store;
       if (!px && pos != mine) {  // another P loader's message: only count it
-        if (m.in) {
-          ++m_in;
+        if (m.in) ++m_in;
+        if (slot_recv) {
+          ++s_in;
           if (++slot_in == (uint32_t)K) slot_in = 0;
         }
-        if (m.send) ++m_out;
+        if (slot_send) ++s_out;
         continue;
       }
       int ok = 1;
@@ -370,8 +392,8 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
           const uint64_t want = E | (uint64_t)(m_in + 1);
           if (seen_head < want) ok = wait_geq(head_in, want, &seen_head, a.wait, tag, r, prev, (int)q);
         }
-        if (m.send && lane == 1 && m_out >= (uint32_t)K) {
-          const uint64_t want = E | (uint64_t)(m_out - K + 1);
+        if (slot_send && lane == 1 && s_out >= (uint32_t)K) {
+          const uint64_t want = E | (uint64_t)(s_out - K + 1);
           if (seen_tail < want) ok = wait_geq(tail_out, want, &seen_tail, a.wait, tag, r, next, (int)q);
         }
       }
@@ -385,18 +407,24 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
             bulk_load_stream(xbuf + (size_t)st.b * xstage,
                              static_cast<const char*>(a.in[r]) + (a.ibase[m.c] + m.base * PU) * ES, bytes, &full[st.b]);
         } else {
-          const uint32_t bytes = m.in ? m.units * 16u * (uint32_t)m.nw : 0u;
+          // a partial from the slot, or a value (whole units) from the
+          // sender's output
+          const uint32_t bytes = !m.in ? 0u : (slot_recv ? m.units * 16u * (uint32_t)m.nw : m.xfull * 16u);
           if (bytes) fence_proxy_async_global();  // generic-proxy writes acquired above, read by the async proxy
           c_mbar_arrive_tx(&full[st.b], bytes);
-          if (bytes)
+          if (bytes && slot_recv)
             c_bulk_load(pbuf + (size_t)st.b * pstage, fifo_in + (size_t)slot_in * a.slot_bytes, bytes, &full[st.b]);
+          else if (bytes)
+            c_bulk_load(pbuf + (size_t)st.b * pstage,
+                        static_cast<const char*>(a.out[prev]) + (a.obase[m.c] + m.base * PU) * ES, bytes, &full[st.b]);
         }
       }
-      if (m.in) {
-        ++m_in;
+      if (m.in) ++m_in;
+      if (slot_recv) {
+        ++s_in;
         if (++slot_in == (uint32_t)K) slot_in = 0;
       }
-      if (m.send) ++m_out;
+      if (slot_send) ++s_out;
     }
     if (q < Q && lane == 0) {
       *abort = 1;
@@ -450,9 +478,10 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
     const int tid = cw * 32 + lane;
     StagedCursor k;
     StagedStage st;
-    uint32_t m_in = 0, slot_out = 0;
+    uint32_t s_in = 0, slot_out = 0;  // partials received; next outgoing slot
     for (uint32_t q = 0; q < Q; ++q, k.next(G, steps), st.next(D)) {
       const StagedMsg m = staged_msg<DT>(a, r, ch, k);
+      const bool slot_recv = m.in && m.x, slot_send = m.send && !m.store;
       int ok = 1;
       if (lane == 0 && !(staged_mbar_wait(&sh.fullx[st.b], st.ph, abort, a.wait.timeout_ns) &&
                          staged_mbar_wait(&sh.fullp[st.b], st.ph, abort, a.wait.timeout_ns))) {
@@ -467,7 +496,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
       // every lane reads the stage: make the completed copies visible to it
       mbar_try_cta(&sh.fullx[st.b], st.ph);
       mbar_try_cta(&sh.fullp[st.b], st.ph);
-      if (m.in && tid == 0) red_max_relaxed(tail_in, E | (uint64_t)(m_in + 1));  // slot copied out: credit
+      if (slot_recv && tid == 0) red_max_relaxed(tail_in, E | (uint64_t)(s_in + 1));  // slot copied out: credit
       const unsigned char* xs = xbuf + (size_t)st.b * xstage;
       const unsigned char* ps = pbuf + (size_t)st.b * pstage;
       char* so = fifo_out + (size_t)slot_out * a.slot_bytes;
@@ -477,22 +506,23 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
         // stage first, then adds, then stores
         for (uint32_t u0 = tid; u0 < m.units; u0 += kStagedNT * staged_batch<DT>()) {
           if (!m.x)
-            staged_forward<DT>(ps, so, yg, m.base, u0, m.units, m.send);
+            staged_forward<DT>(ps, yg, m.base, u0, m.units, m.send);
           else if (!m.store)
             staged_partial<DT>(xs, ps, so, u0, m.units, m.in);
           else
-            staged_final<DT>(xs, ps, so, yg, m.base, u0, m.units, m.in, m.send);
+            staged_final<DT>(xs, ps, yg, m.base, u0, m.units, m.in, m.send);
         }
       } else {
-        staged_ragged<DT>(m, xs, ps, so, static_cast<const char*>(a.in[r]) + a.ibase[m.c] * ES, yg, a.len[m.c], tid);
+        staged_ragged<DT>(m, xs, ps, so, static_cast<const char*>(a.in[r]) + a.ibase[m.c] * ES,
+                          static_cast<const char*>(a.out[prev]) + a.obase[m.c] * ES, yg, a.len[m.c], tid);
       }
       __syncwarp();
       if (lane == 0) {
         c_mbar_arrive_tx(&sh.empty[st.b], 0);  // this warp no longer reads the stage
         st_release_cta_u32(&sh.done[cw], q + 1);
       }
-      if (m.in) ++m_in;
-      if (m.send && ++slot_out == (uint32_t)K) slot_out = 0;
+      if (slot_recv) ++s_in;
+      if (slot_send && ++slot_out == (uint32_t)K) slot_out = 0;
     }
   }
   arrive_end(a.wait.sync, epoch);

@@ -303,9 +303,9 @@ int ring_form(size_t chunk_bytes, bool staged_ok) {
 constexpr size_t kStagedSmemBudget = 200u << 10;  // dynamic shared memory for the stages
 
 // Staged ring: messages of T units, G per step, K slots per link, D stages.
-// Defaults (measured on GB300, 8 ranks x 100 MB per rank): T up to 2048
-// units and G = 6 for 4-byte types, T up to 1024 and G = 8 for bfloat16
-// (whose partials travel as float32); K = 2G.  Larger G fills L2 with FIFO
+// Defaults (measured on GB300, 8 ranks x 100 MB per rank): G = 6, T up to
+// 2048 units for 4-byte types and up to 1536 for bfloat16 (whose partials
+// travel as float32); K = 2G.  Larger G fills L2 with FIFO
 // slots (links x K x slot bytes) and runs slower.  Channels: as many as the GPU holds, but no more than
 // leave G tiles of 128 units each; then T is the smallest multiple of 32
 // units that covers the chunk in whole iterations, so no iteration runs
@@ -317,8 +317,8 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
   // G: the default, or fewer when the chunk fills fewer than G tiles of 128
   // units per channel (every message of a step costs a hop, even empty)
   const size_t gfill = (maxu + (size_t)s->sms / n * 128 - 1) / std::max<size_t>(1, (size_t)s->sms / n * 128);
-  a.G = (int)std::max(1L, env_long("RRA_RING_G", std::min<long>(aw == 2 ? 8 : 6, (long)std::max<size_t>(1, gfill))));
-  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_RING_TILE", aw == 2 ? 1024 : 2048)));
+  a.G = (int)std::max(1L, env_long("RRA_RING_G", std::min<long>(6, (long)std::max<size_t>(1, gfill))));
+  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_RING_TILE", aw == 2 ? 1536 : 2048)));
   auto stages_for = [&](long t) {
     const long d = (long)(kStagedSmemBudget / ((size_t)t * 16 * (1 + aw)));
     return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_RING_STAGES", 8)}));

@@ -64,15 +64,19 @@ def test_floor_bytes_and_bus_factors():
     assert bench.bus_factor("ar_x", 8) == model.bus_factor("allreduce", 8)
     assert bench.bus_factor("rs_x", 8) == model.bus_factor("reducescatter", 8)
     assert bench.bus_factor("ag_x", 8) == model.bus_factor("allgather", 8)
-    # the ring's L2 bytes: inputs and outputs once, each of 2(n-1) sends per
-    # rank through a slot (written, read back) -- 44 S at n = 8 for 4-byte types;
-    # the per-rank send count is the oracle's ring traffic, 2(n-1)/n S per rank
-    assert bench.ring_l2_bytes(8, S) == 44 * S
-    assert bench.ring_l2_bytes(2, S) == 8 * S
-    # pinned to the oracle's byte counters of an actual ring all-reduce
+    # the ring's L2 bytes: inputs and outputs once, each reduce-scatter send
+    # through a slot (written, read back), each forwarded value read once from
+    # the sender's output -- 37 S at n = 8 for 4-byte types
+    assert bench.ring_l2_bytes(8, S) == 37 * S
+    assert bench.ring_l2_bytes(2, S) == 7 * S
+    # pinned to the oracle's byte counters of an actual ring all-reduce: its
+    # reduce-scatter half sends the partials, the rest are forwarded values
     import numpy as np
     import oracle
 
     xs = [np.full(800, k, dtype=np.int32) for k in range(8)]
     _, sent, _ = oracle.allreduce("ring", xs, "int32")
-    assert bench.ring_l2_bytes(8, 800 * 4) == 2 * 8 * 800 * 4 + 2 * int(np.sum(sent))
+    _, sent_rs, _ = oracle.reduce_scatter("ring", xs, "int32")
+    partials, values = int(np.sum(sent_rs)), int(np.sum(sent)) - int(np.sum(sent_rs))
+    assert partials == values == 7 * 800 * 4
+    assert bench.ring_l2_bytes(8, 800 * 4) == 2 * 8 * 800 * 4 + 2 * partials + values

@@ -1,6 +1,13 @@
 """A discrete-event model of the staged ring's link protocol
 (kernels_ring_staged.cu), run on the CPU under random interleavings.
 
+Reduce-scatter partials travel through the link's FIFO slots (credits
+bound the sender); a value in the element type -- the finished chunk the
+last reduce-scatter step forwards, and every all-gather forward -- is not
+copied into a slot: the sender stores it in its own output and posts it,
+and the receiver reads it from there (an output is never rewritten within
+a call, so it needs no credit).  The head counter counts every message.
+
 The model has the same roles and waits as the kernel: per virtual rank an X
 loader, P loaders taking messages round-robin, in-order consumers and a
 signaller; per stage "full" and "empty" mbarriers tested by phase parity;
@@ -58,13 +65,20 @@ def run_model(n, mode, G, K, D, P, iters, seed, cap_loaders=True):
     seq = messages(n, mode, G, iters)
     Q = len(seq)
     npl = min(P, D) if cap_loaders else P
-    rin, rout = [], []  # receive / send ordinal of each message
-    a = b = 0
+    rin, rout = [], []  # receive / send ordinal of each message (head counter)
+    srin, srout = [], []  # ordinal among slot messages (partials)
+    a = b = c = d = 0
     for m in seq:
+        m["slot_in"] = m["inn"] and m["kind"] in ("rs", "fin")
+        m["slot_out"] = m["send"] and m["kind"] == "rs"
         rin.append(a)
         rout.append(b)
+        srin.append(c)
+        srout.append(d)
         a += m["inn"]
         b += m["send"]
+        c += m["slot_in"]
+        d += m["slot_out"]
     X = [0] * n
     Pq = [list(range(npl)) for _ in range(n)]  # next message of each P loader
     C = [0] * n
@@ -104,7 +118,7 @@ def run_model(n, mode, G, K, D, P, iters, seed, cap_loaders=True):
                 m = seq[q]
                 if m["inn"] and head[(r - 1) % n] < rin[q] + 1:
                     continue
-                if m["send"] and rout[q] >= K and tail[r] < rout[q] - K + 1:
+                if m["slot_out"] and srout[q] >= K and tail[r] < srout[q] - K + 1:
                     continue
                 acts.append(("P", r, p))
             q = C[r]
@@ -124,10 +138,15 @@ def run_model(n, mode, G, K, D, P, iters, seed, cap_loaders=True):
             X[r] += 1
         elif kind == "P":
             q = Pq[r][p]
-            if seq[q]["inn"]:
-                sl = slots[(r - 1) % n][rin[q] % K]
-                assert sl is not None and sl[0] == rin[q], ("slot not yet written or reused", r, q)
+            m = seq[q]
+            if m["slot_in"]:
+                sl = slots[(r - 1) % n][srin[q] % K]
+                assert sl is not None and sl[0] == srin[q], ("slot not yet written or reused", r, q)
                 stage_p[r][q % D] = sl[1]
+            elif m["inn"]:  # pulled from the sender's output
+                key = (chunk_of(m, r, n), m["it"], m["g"])
+                assert key in out[(r - 1) % n], ("output read before it was posted", r, q)
+                stage_p[r][q % D] = (key, out[(r - 1) % n][key])
             fullp[r][q % D] += 1
             Pq[r][p] += npl
         elif kind == "C":
@@ -137,15 +156,16 @@ def run_model(n, mode, G, K, D, P, iters, seed, cap_loaders=True):
             contrib = []
             if m["inn"]:
                 val = stage_p[r][q % D]
-                tail[(r - 1) % n] = max(tail[(r - 1) % n], cin[r] + 1)  # credit once copied out
-                cin[r] += 1
+                if m["slot_in"]:
+                    tail[(r - 1) % n] = max(tail[(r - 1) % n], cin[r] + 1)  # credit once copied out
+                    cin[r] += 1
                 assert val[0] == key, ("wrong message", val, key)
                 contrib = list(val[1])
             if m["x"]:
                 contrib.append(r)
             if m["store"]:
                 out[r][key] = tuple(contrib)
-            if m["send"]:
+            if m["slot_out"]:
                 slots[r][cout[r] % K] = (cout[r], (key, tuple(contrib)))
                 cout[r] += 1
             empty[r][q % D] += 1
