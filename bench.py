@@ -568,19 +568,27 @@ def oracle_step(oracle, host, flag):
     oracle.ll128_unpack(w, B, "int32", flag)
 
 
+def sample_sizes(share):
+    """Bucket elements per rank and LL payload bytes of a 1/share sample,
+    rounded down to whole chunks (a multiple of the rank count) and whole
+    16-byte groups."""
+    count = max(N_RANKS, BUCKET // share // N_RANKS * N_RANKS)
+    return count, max(16, LL_BYTES // share // 16 * 16)
+
+
 def sample_host(scale, seed=0):
     from collective_all_reduce_rank_gb300 import inputs
 
-    count = BUCKET // scale
+    count, llb = sample_sizes(scale)
     xs = inputs.cfg_gradient_bucket(count, seed=seed)
     return {"bucket": xs, "shards": [x[: count // N_RANKS].copy() for x in xs],
-            "payloads": inputs.cfg_ll_payloads(LL_BYTES // scale, LL_SRC, seed=seed)}
+            "payloads": inputs.cfg_ll_payloads(llb, LL_SRC, seed=seed)}
 
 
 def sample_floor(scale):
     n = N_RANKS
-    S = (BUCKET // scale) * 4
-    B = LL_BYTES // scale
+    count, B = sample_sizes(scale)
+    S = count * 4
     LW, L8 = 8 * ((B + 3) // 4), 128 * ((B + 119) // 120)
     return (3 * floor_bytes("ar_", n, S) + 2 * floor_bytes("rs_", n, S) + 2 * floor_bytes("ag_", n, S)
             + LL_SRC * (B + LW) + LL_SRC * LW + B + LL_SRC * (B + L8) + LL_SRC * L8 + B)
@@ -607,17 +615,65 @@ def host_cpu():
     return {"cpu_model": model, "host_cores_available": avail}
 
 
-def cpu_baseline(scale):
+def cpu_baseline(scale, min_s=10.0, max_steps=8):
+    """The oracle on one core: steps at 1/scale of the workload, repeated
+    until about `min_s` seconds of CPU work (at most `max_steps`)."""
     import oracle
 
     host = sample_host(scale)
-    t = time.perf_counter()
-    oracle_step(oracle, host, 1)
-    dt = time.perf_counter() - t
-    return {"value": round(sample_floor(scale) / dt / 1e9, 3), "unit": UNIT, "cores": 1,
+    count, llb = sample_sizes(scale)
+    steps, t = 0, time.perf_counter()
+    while True:
+        oracle_step(oracle, host, steps + 1)
+        steps += 1
+        dt = time.perf_counter() - t
+        if dt >= min_s or steps >= max_steps:
+            break
+    return {"value": round(steps * sample_floor(scale) / dt / 1e9, 3), "unit": UNIT, "cores": 1,
             "kind": "oracle", "seconds": round(dt, 2), **host_cpu(),
-            "sample": "one step at 1/%d of the workload (bucket %d elems/rank, LL payload %d B), "
-                      "single-threaded C oracle" % (scale, BUCKET // scale, LL_BYTES // scale)}
+            "sample": "%d steps at 1/%d of the workload (bucket %d elems/rank, LL payload %d B), "
+                      "single-threaded C oracle" % (steps, scale, count, llb),
+            "all_cores": cpu_baseline_all_cores(scale)}
+
+
+def cpu_baseline_all_cores(scale, min_s=2.0, max_rounds=50):
+    """The same oracle on every host core this process may use: T threads,
+    each running steps on its own independent 1/T share of the sample
+    (every element's reduction is independent, so the shares are separate
+    problems of the same shape; the C oracle releases the GIL), repeated
+    until about `min_s` seconds of wall time."""
+    import threading
+
+    import oracle
+
+    T = max(1, min(16, host_cpu()["host_cores_available"] or 1))
+    hosts = [sample_host(scale * T, seed=t) for t in range(T)]
+    oracle_step(oracle, sample_host(scale * T * 16, seed=T), 1)  # load and build outside the clock
+    errs = []
+
+    def work(h, k):
+        try:
+            oracle_step(oracle, h, k)
+        except Exception as e:  # reported below, not swallowed
+            errs.append(e)
+
+    rounds, t = 0, time.perf_counter()
+    while not errs:
+        threads = [threading.Thread(target=work, args=(h, rounds + 1)) for h in hosts]
+        for th in threads:
+            th.start()
+        for th in threads:
+            th.join()
+        rounds += 1
+        dt = time.perf_counter() - t
+        if dt >= min_s or rounds >= max_rounds:
+            break
+    if errs:
+        raise errs[0]
+    return {"value": round(rounds * T * sample_floor(scale * T) / dt / 1e9, 3), "unit": UNIT, "cores": T,
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": "%d threads x %d steps, each on its own 1/%d of the workload; single-threaded "
+                      "C oracle per thread" % (T, rounds, scale * T)}
 
 
 FULL_STEP_CPU_S = 26.0  # one oracle step at full size on one core, measured

@@ -80,3 +80,21 @@ def test_floor_bytes_and_bus_factors():
     partials, values = int(np.sum(sent_rs)), int(np.sum(sent)) - int(np.sum(sent_rs))
     assert partials == values == 7 * 800 * 4
     assert bench.ring_l2_bytes(8, 800 * 4) == 2 * 8 * 800 * 4 + 2 * partials + values
+
+
+def test_cpu_baseline_samples():
+    import bench
+
+    # samples are whole chunks and whole 16-byte LL groups at any share
+    for share in (1, 2, 3, 7, 24, 64, 1 << 20):
+        count, llb = bench.sample_sizes(share)
+        assert count % bench.N_RANKS == 0 and count >= bench.N_RANKS
+        assert llb % 16 == 0 and llb >= 16
+    assert bench.sample_sizes(1) == (bench.BUCKET, bench.LL_BYTES)
+    # T independent shares carry the sample's floor bytes, up to the rounding
+    full = bench.sample_floor(2)
+    for T in (3, 8, 16):
+        assert abs(T * bench.sample_floor(2 * T) - full) / full < 1e-4
+    # the all-cores variant runs the oracle on every share and reports its threads
+    r = bench.cpu_baseline_all_cores(4096, min_s=0.0, max_rounds=1)
+    assert r["kind"] == "oracle" and r["cores"] >= 1 and r["value"] > 0
