@@ -12,20 +12,23 @@
 // the same bits.  bfloat16 partials travel as float32.
 //
 // One persistent cooperative launch of n x C CTAs; CTA (r, ch) is channel ch
-// of rank r.  Per channel each node owns an up FIFO (its partials, read by
-// its parent) and, when it has children, one down FIFO (the totals, written
-// once and read by both children); each FIFO has K slots in the workspace,
-// a head counter (messages posted) and one tail counter per reader
-// (messages copied out).  A node's messages, per iteration of G tiles of T
-// units: its G up messages, then -- not at the root -- the G down messages
-// of the previous iteration, so one iteration's broadcast overlaps the next
-// one's reduction.  Warp roles as in the staged ring: an X loader
-// (bulk-copies the node's own input tile), P loaders (acquire the heads of
-// the incoming links and the tails of the outgoing one, then bulk-copy the
-// children's or the parent's slots; at most as many as stages, so the
-// stage mbarriers' parity tests stay sound), consumers (add, write the
-// outgoing slot and the output), and a signaller (one fence per run of
-// finished messages, then the head counters).  Every wait is bounded.
+// of rank r.  Per channel each non-root node owns an up FIFO (its partials,
+// read by its parent) of K slots in the workspace, with a head counter
+// (messages posted) and a tail counter (messages the parent has copied
+// out).  The totals going down need no FIFO: a node with children stores
+// the total in its own output, kept in L2, and posts it on its down head
+// counter; both children bulk-copy it from there (an output is written once
+// per call, so these reads need no credit).  A node's messages, per
+// iteration of G tiles of T units: its G up messages, then -- not at the
+// root -- the G down messages of iteration it - L, so the broadcast of one
+// iteration overlaps the reduction of the next L.  Warp roles as in the staged
+// ring: an X loader (bulk-copies the node's own input tile), P loaders
+// (acquire the heads of the incoming links and the tail of the up link,
+// then bulk-copy the children's slots or the parent's output; at most as
+// many as stages, so the stage mbarriers' parity tests stay sound),
+// consumers (add, write the up slot or the output), and a signaller (one
+// fence per run of finished messages, then the head counters).  Every wait
+// is bounded.
 //
 // Needs 16-byte aligned buffers.  The last tile's partial 16-byte unit is
 // read and written element-wise by the consumers.
@@ -43,20 +46,26 @@ constexpr int kTreeNT = kTreeConsumers * 32;
 
 // Position in a node's message sequence: iteration `it`, phase (0 = up
 // messages of tile iteration it, 1 = down messages of tile iteration
-// it - 1), slice g.
+// it - L), slice g.  The down messages trail by L iterations; once the ups
+// are done, the remaining downs follow.
 struct TreeCursor {
   uint32_t it = 0, ph = 0, g = 0;
-  __device__ __forceinline__ void next(int G, uint32_t iters, bool root) {
+  __device__ __forceinline__ void next(int G, uint32_t iters, bool root, uint32_t L) {
     if (++g < (uint32_t)G) return;
     g = 0;
-    if (ph == 0 && !root && it >= 1) {
-      ph = 1;  // down messages of the previous iteration
+    if (ph == 0 && !root && it >= L) {
+      ph = 1;  // the downs of iteration it - L
       return;
     }
     ++it;
-    ph = (!root && it == iters) ? 1u : 0u;  // after the last up: the last down
+    if (it >= iters) {
+      if (it < L) it = L;
+      ph = 1;
+    } else {
+      ph = 0;
+    }
   }
-  __device__ __forceinline__ uint32_t tile_it() const { return ph == 0 ? it : it - 1; }
+  __device__ __forceinline__ uint32_t tile_it(uint32_t L) const { return ph == 0 ? it : it - L; }
 };
 
 struct TreeShared {
@@ -95,11 +104,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ TreeShared sh;
   const int n = a.n, C = a.channels, G = a.G, K = a.K, D = a.stages, T = a.slice_units;
+  const uint32_t L = (uint32_t)a.lag;
   const int r = blockIdx.x % n, ch = blockIdx.x / n;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool root = r == 0;
   const int parent = root ? 0 : (r - 1) / 2;
-  const int side = root ? 0 : (r == 2 * parent + 1 ? 0 : 1);  // which child of its parent
   const int nk = (2 * r + 1 < n) + (2 * r + 2 < n);           // children
   const size_t xstage = (size_t)T * 16, pstage = (size_t)T * 16 * AW;
   unsigned char* xbuf = smem;                                 // [D][T] units
@@ -128,20 +137,20 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
   const uint32_t iters = (uint32_t)((units + per_iter_units - 1) / per_iter_units);
   const uint32_t Q = iters * (uint32_t)G * (root ? 1u : 2u);
   auto tile_of = [&](const TreeCursor& k, uint32_t* nu, uint32_t* nx) -> size_t {
-    const size_t base = (((size_t)k.tile_it() * C + ch) * G + k.g) * (size_t)T;
+    const size_t base = (((size_t)k.tile_it(L) * C + ch) * G + k.g) * (size_t)T;
     *nu = base < units ? (uint32_t)(units - base < (size_t)T ? units - base : (size_t)T) : 0u;
     *nx = base < whole ? (uint32_t)(whole - base < (size_t)T ? whole - base : (size_t)T) : 0u;
     return base;
   };
 
-  // links of this CTA (per channel): FIFO slots, heads, tails
+  // links of this CTA (per channel): up FIFO slots, heads, up tails
   const size_t link_stride = (size_t)K * a.slot_bytes;
   auto up_fifo = [&](int node) { return a.fifo + ((size_t)node * C + ch) * link_stride; };
-  auto dn_fifo = [&](int node) { return a.fifo + ((size_t)(n + node) * C + ch) * link_stride; };
   auto up_head = [&](int node) { return a.head + (size_t)node * C + ch; };
   auto dn_head = [&](int node) { return a.head + (size_t)(n + node) * C + ch; };
   auto up_tail = [&](int node) { return a.tail + (size_t)node * C + ch; };
-  auto dn_tail = [&](int node, int k) { return a.tail + ((size_t)(1 + k) * n + node) * C + ch; };
+  // the parent's output: the totals coming down
+  const char* pg = static_cast<const char*>(a.out[parent]);
   const int c1 = 2 * r + 1, c2 = 2 * r + 2;
   const bool active = r != a.wait.skip_rank;
   // joined flags: each CTA marks its (rank, channel) for this call before
@@ -160,20 +169,19 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     uint64_t* full = px ? sh.fullx : sh.fullp;
     TreeCursor k;
     StagedStage st;
-    uint32_t up_in = 0, dn_in = 0, up_out = 0, dn_out = 0;
+    uint32_t up_in = 0, dn_in = 0, up_out = 0;
     // last value seen of each polled counter: children's up heads (0, 1),
-    // the up link's tail (2), the down link's tails (3, 4), the parent's
-    // down head (5) -- one cache per counter, never shared between two
-    uint64_t seen[6] = {0, 0, 0, 0, 0, 0};
+    // the up link's tail (2), the parent's down head (3) -- one cache per
+    // counter, never shared between two
+    uint64_t seen[4] = {0, 0, 0, 0};
     uint32_t q = 0;
     if (mine >= np) q = Q;
-    for (; q < Q; ++q, k.next(G, iters, root), st.next(D), pos = pos + 1 == np ? 0u : pos + 1) {
+    for (; q < Q; ++q, k.next(G, iters, root, L), st.next(D), pos = pos + 1 == np ? 0u : pos + 1) {
       const bool up = k.ph == 0;
       uint32_t nu, nx;
       const size_t base = tile_of(k, &nu, &nx);
       const bool has_in = up ? nk > 0 : true;
       const bool send_up = up && !root;
-      const bool send_dn = up ? (root && nk > 0) : nk > 0;
       if (!px && pos != mine) {  // another P loader's message: only count it
         if (up) {
           if (nk > 0) ++up_in;
@@ -181,7 +189,6 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
         } else {
           ++dn_in;
         }
-        if (send_dn) ++dn_out;
         continue;
       }
       int ok = 1;
@@ -190,8 +197,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
         ok = 0;
       }
       if (!px && ok) {
-        // lanes 0/1: incoming heads (children, or the parent); lanes 2..4:
-        // the outgoing link's tails; side by side
+        // lanes 0/1: incoming heads (children, or the parent); lane 2: the
+        // up link's tail; side by side
         const uint64_t* f = nullptr;
         uint64_t want = 0;
         int peer = -1, slot = 0;
@@ -204,17 +211,12 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
           f = dn_head(parent);
           want = E | (uint64_t)(dn_in + 1);
           peer = parent;
-          slot = 5;
+          slot = 3;
         } else if (lane == 2 && send_up && up_out >= (uint32_t)K) {
           f = up_tail(r);
           want = E | (uint64_t)(up_out - K + 1);
           peer = parent;
           slot = 2;
-        } else if (lane >= 3 && lane < 3 + nk && send_dn && dn_out >= (uint32_t)K) {
-          f = dn_tail(r, lane - 3);
-          want = E | (uint64_t)(dn_out - K + 1);
-          peer = lane == 3 ? c1 : c2;
-          slot = lane;
         }
         if (f && seen[slot] < want) ok = wait_geq(f, want, &seen[slot], a.wait, tag, r, peer, (int)q, joined(peer));
       }
@@ -228,7 +230,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
             bulk_load_stream(xbuf + (size_t)st.b * xstage, static_cast<const char*>(a.in[r]) + base * 16, bytes,
                              &full[st.b]);
         } else {
-          const uint32_t each = up ? nu * 16u * (uint32_t)AW : nu * 16u;
+          // partials: every unit of the tile from each child's slot; the
+          // total: the whole units from the parent's output
+          const uint32_t each = up ? nu * 16u * (uint32_t)AW : nx * 16u;
           const uint32_t bytes = has_in ? each * (up ? (uint32_t)nk : 1u) : 0u;
           if (bytes) fence_proxy_async_global();
           c_mbar_arrive_tx(&full[st.b], bytes);
@@ -238,8 +242,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
               c_bulk_load(p1buf + (size_t)st.b * pstage, up_fifo(c1) + so, each, &full[st.b]);
               if (nk > 1) c_bulk_load(p2buf + (size_t)st.b * pstage, up_fifo(c2) + so, each, &full[st.b]);
             } else {
-              c_bulk_load(p1buf + (size_t)st.b * pstage, dn_fifo(parent) + (size_t)(dn_in % (uint32_t)K) * a.slot_bytes,
-                          each, &full[st.b]);
+              c_bulk_load(p1buf + (size_t)st.b * pstage, pg + base * 16, each, &full[st.b]);
             }
           }
         }
@@ -250,7 +253,6 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
       } else {
         ++dn_in;
       }
-      if (send_dn) ++dn_out;
     }
     if (q < Q && lane == 0) {
       *abort = 1;
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
       for (int o = 16; o > 0; o >>= 1) d = min(d, __shfl_xor_sync(0xffffffffu, d, o));
       if (d > q) {
         uint32_t nup = 0, ndn = 0;
-        for (; q < d; ++q, k.next(G, iters, root)) {
+        for (; q < d; ++q, k.next(G, iters, root, L)) {
           const bool up = k.ph == 0;
           if (up && !root) ++nup;
           if (up ? (root && nk > 0) : nk > 0) ++ndn;
@@ -307,10 +309,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     const int tid = cw * 32 + lane;
     TreeCursor k;
     StagedStage st;
-    uint32_t up_in = 0, dn_in = 0, up_slot = 0, dn_slot = 0;
+    uint32_t up_in = 0, up_slot = 0;
     const char* xg = static_cast<const char*>(a.in[r]);
     char* yg = static_cast<char*>(a.out[r]);
-    for (uint32_t q = 0; q < Q; ++q, k.next(G, iters, root), st.next(D)) {
+    for (uint32_t q = 0; q < Q; ++q, k.next(G, iters, root, L), st.next(D)) {
       const bool up = k.ph == 0;
       uint32_t nu, nx;
       const size_t base = tile_of(k, &nu, &nx);
@@ -329,28 +331,26 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
       }
       mbar_try_cta(&sh.fullx[st.b], st.ph);
       mbar_try_cta(&sh.fullp[st.b], st.ph);
-      // incoming slots copied out: credits
-      if (tid == 0) {
-        if (up && nk > 0) {
-          red_max_relaxed(up_tail(c1), E | (uint64_t)(up_in + 1));
-          if (nk > 1) red_max_relaxed(up_tail(c2), E | (uint64_t)(up_in + 1));
-        } else if (!up) {
-          red_max_relaxed(dn_tail(parent, side), E | (uint64_t)(dn_in + 1));
-        }
+      // the children's slots copied out: credits
+      if (tid == 0 && up && nk > 0) {
+        red_max_relaxed(up_tail(c1), E | (uint64_t)(up_in + 1));
+        if (nk > 1) red_max_relaxed(up_tail(c2), E | (uint64_t)(up_in + 1));
       }
       const unsigned char* xs = xbuf + (size_t)st.b * xstage;
       const unsigned char* p1 = p1buf + (size_t)st.b * pstage;
       const unsigned char* p2 = p2buf + (size_t)st.b * pstage;
-      char* so = send_up ? up_fifo(r) + (size_t)up_slot * a.slot_bytes
-                         : (send_dn ? dn_fifo(r) + (size_t)dn_slot * a.slot_bytes : nullptr);
+      char* so = send_up ? up_fifo(r) + (size_t)up_slot * a.slot_bytes : nullptr;
       for (uint32_t u = tid; u < nu; u += kTreeNT) {
         const size_t gu = base + u;
         const int v = unit_valid<DT>(gu, a.count);
         if (!up) {
-          // the total, in the element type, from the parent
-          const uint4 val = lds128(p1 + (size_t)u * 16);
-          store_out<DT, true, true>(yg, gu, v, val);
-          if (send_dn) st_l2(so + (size_t)u * 16, val);
+          // the total, in the element type, from the parent's output; kept
+          // in L2 when the children will read it
+          const uint4 val = u < nx ? lds128(p1 + (size_t)u * 16) : ld_partial_l2<DT>(pg + gu * 16, v);
+          if (send_dn)
+            store_out<DT, true, false>(yg, gu, v, val);
+          else
+            store_out<DT, true, true>(yg, gu, v, val);
           continue;
         }
         Acc s;
@@ -374,8 +374,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
         } else {
           // root: the total, rounded once
           const uint4 val = acc_narrow<DT>(s);
-          store_out<DT, true, true>(yg, gu, v, val);
-          if (send_dn) st_l2(so + (size_t)u * 16, val);
+          if (send_dn)
+            store_out<DT, true, false>(yg, gu, v, val);
+          else
+            store_out<DT, true, true>(yg, gu, v, val);
         }
       }
       __syncwarp();
@@ -386,10 +388,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
       if (up) {
         if (nk > 0) ++up_in;
         if (send_up && ++up_slot == (uint32_t)K) up_slot = 0;
-      } else {
-        ++dn_in;
       }
-      if (send_dn && ++dn_slot == (uint32_t)K) dn_slot = 0;
     }
   }
   arrive_end(a.wait.sync, epoch);

@@ -355,13 +355,16 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
   return cuda_status(launch_ring_staged(dt, a, n * (int)c, st));
 }
 
-// Staged tree: one message per tile of T units (T <= RRA_TREE_TILE: 1024 for
-// 4-byte types, 512 for bfloat16, whose partials travel as float32), G tiles
-// per iteration (RRA_TREE_G, 24), K = G + 1 FIFO slots per link
-// (RRA_TREE_K), stages as shared memory allows; T balanced over whole
-// iterations as in the staged ring.  Measured on GB300 at 8 x 100 MB: G
-// hides the up-and-back wave of each iteration (G = 4: 0.86 TB/s, 16: 1.58,
-// 24: 1.77, 32: 1.56, when the FIFO crowds L2).
+// Staged tree: one message per tile of T units (T <= RRA_TREE_TILE: 2048 for
+// 4-byte types, 1024 for bfloat16, whose partials travel as float32), G
+// tiles per iteration (RRA_TREE_G, 24), K = G + 1 FIFO slots per up link
+// (RRA_TREE_K), the broadcast L iterations behind the reduction
+// (RRA_TREE_LAG: 6, 4 for bfloat16), stages as shared memory allows; T
+// balanced over whole iterations as in the staged ring.  Measured on GB300
+// at 8 x 100 MB fp32: larger tiles pay for fewer stages (T 1024: 1.77 TB/s,
+// 2048: 2.25); G hides the up-and-back wave of each iteration until the
+// FIFO crowds L2 (G 12: 1.95, 24: 2.25, 32: 2.04 at T 2048); a lag of 6
+// gives 2.48.
 rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* out, int n, size_t count,
                              rra_dtype_t dt, cudaStream_t st, int* grid_out) {
   StagedTreeArgs a{};
@@ -374,7 +377,8 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   a.count = count;
   const size_t units = (count * e + 15) / 16;
   a.G = (int)std::max(1L, env_long("RRA_TREE_G", 24));
-  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_TREE_TILE", aw == 2 ? 512 : 1024)));
+  a.lag = (int)std::max(1L, std::min(64L, env_long("RRA_TREE_LAG", aw == 2 ? 4 : 6)));
+  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_TREE_TILE", aw == 2 ? 1024 : 2048)));
   auto stages_for = [&](long t) {
     const long d = (long)(kStagedSmemBudget / ((size_t)t * 16 * (1 + 2 * aw)));
     return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_TREE_STAGES", 8)}));
@@ -397,9 +401,10 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   a.slot_bytes = (size_t)T * 16 * aw;
   a.K = (int)std::max((long)a.G + 1, env_long("RRA_TREE_K", (long)a.G + 1));
-  if ((size_t)c * 2 * n * a.K * a.slot_bytes > s->ws.fifo_bytes) a.K = a.G + 1;
-  c = std::min<long>(c, (long)(s->ws.fifo_bytes / ((size_t)2 * n * a.K * a.slot_bytes)));
-  if (c < 1 || (size_t)3 * n * c > kLinkFlags) return RRA_ERR_UNSUPPORTED;
+  // one up FIFO per node and channel (the totals come down from outputs)
+  if ((size_t)c * n * a.K * a.slot_bytes > s->ws.fifo_bytes) a.K = a.G + 1;
+  c = std::min<long>(c, (long)(s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes)));
+  if (c < 1 || (size_t)2 * n * c > kLinkFlags) return RRA_ERR_UNSUPPORTED;
   const size_t trips = (units + (size_t)c * a.G * T - 1) / ((size_t)c * a.G * T);
   if (trips * 2 * (size_t)a.G >= (1ull << 31)) return RRA_ERR_UNSUPPORTED;
   a.channels = (int)c;

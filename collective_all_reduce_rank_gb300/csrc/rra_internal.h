@@ -123,7 +123,7 @@ struct StagedTreeArgs {
   const void* in[kMaxRanks];
   void* out[kMaxRanks];
   size_t count;  // elements per rank
-  char* fifo;    // 2n links x channels x K slots x slot_bytes
+  char* fifo;    // n up links x channels x K slots x slot_bytes
   uint64_t* head;
   uint64_t* tail;
   uint64_t* joined;  // [n x channels]: the call's epoch once the CTA has started
@@ -134,6 +134,7 @@ struct StagedTreeArgs {
   int G;            // tiles per iteration
   int K;            // FIFO slots per link
   int stages;       // shared-memory stages per CTA
+  int lag;          // iterations the broadcast trails the reduction by (>= 1)
   WaitCfg wait;
 };
 

@@ -66,6 +66,29 @@ def test_staged_tree_shapes(tile, G, K, stages, dtype, n, count, monkeypatch):
             g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "staged tree n=%d r=%d" % (n, r))
 
 
+@pytest.mark.parametrize("lag", [2, 3, 9])
+@pytest.mark.parametrize("tile,G,K,stages", [(256, 3, 4, 2), (1024, 4, 5, 8), (128, 1, 2, 1)])
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("n,count", [(2, 3), (5, 70_001), (8, 8 * 1024 * 4 * 19 + 7), (8, 3_000_001)])
+def test_staged_tree_lag(lag, tile, G, K, stages, dtype, n, count, monkeypatch):
+    # the broadcast trailing the reduction by several iterations (more than
+    # the call has, too): the oracle's tree bits
+    import gpu_util as g
+
+    for k, v in (("RRA_TREE_TILE", tile), ("RRA_TREE_G", G), ("RRA_TREE_K", K), ("RRA_TREE_STAGES", stages),
+                 ("RRA_TREE_LAG", lag)):
+        monkeypatch.setenv(k, str(v))
+    xs = inputs.make_ranks(n, count, dtype, "normal", seed=count + n + lag)
+    want, _, _ = oracle.allreduce("tree", xs, dtype)
+    ins = [g.to_dev(x, dtype) for x in xs]
+    outs = g.empty(n, count, dtype)
+    rra.rra_allreduce(ins, outs, count, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_TREE)
+    st, info = rra.rra_query_status()
+    assert st == 0, info
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "staged tree lag=%d n=%d r=%d" % (lag, n, r))
+
+
 @pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
 @pytest.mark.parametrize("n,count", [(3, 100_003), (8, 3_000_001)])
 def test_cluster_tree_form(dtype, n, count, monkeypatch):

@@ -1,12 +1,14 @@
 """A discrete-event model of the staged tree's link protocol
 (kernels_tree_staged.cu), run on the CPU under random interleavings.
 
-Nodes are virtual ranks in heap order (parent of r is (r-1)/2).  Each node r
-owns an up FIFO (its partial sums, read by its parent) and, when it has
-children, one down FIFO (the final values, read by both children); a FIFO
-has K slots, a head counter (messages posted by the writer's signaller) and
-one tail counter per reader (messages it has copied out); the writer may
-reuse a slot once every reader's tail has passed it.  A node's message
+Nodes are virtual ranks in heap order (parent of r is (r-1)/2).  Each
+non-root node r owns an up FIFO (its partial sums, read by its parent) of K
+slots with a head counter (messages posted by the writer's signaller) and a
+tail counter (messages the parent has copied out); the writer may reuse a
+slot once the tail has passed it.  The totals come down without a FIFO: a
+node with children stores each total in its own output and posts it on its
+down head counter, and both children read it from there (an output is
+written once, so it needs no credit).  A node's message
 sequence is, per iteration of G tiles: its G up messages, then (not at the
 root) the G down messages of the previous iteration, so the down wave of
 one iteration overlaps the up wave of the next.  Per CTA the roles are as
@@ -15,8 +17,9 @@ most as many as stages), in-order consumers, a signaller; stages are
 tested by mbarrier phase parity.
 
 Checked: every run finishes (no deadlock), no slot is read before it is
-written or after it is reused, no parity test passes for a phase that has
-not completed, and every rank ends with the total summed in the order of
+written or after it is reused, no output is read before it is posted, no
+parity test passes for a phase that has not completed, and every rank ends
+with the total summed in the order of
 "Collective communication: NCCL's algorithms and protocols ...", section
 "Algorithms" (tree), as the oracle reads it: p_r = (x_r + p_{2r+1}) + p_{2r+2}.
 """
@@ -29,15 +32,41 @@ class Aliasing(Exception):
     pass
 
 
-def tree_messages(n, r, G, iters):
+def tree_messages(n, r, G, iters, lag=1):
     seq = []
-    for it in range(iters + 1):
+    for it in range(iters + lag):
         if it < iters:
             for g in range(G):
                 seq.append(("up", it, g))
-        if it >= 1 and r > 0:
+        if it >= lag and r > 0:
             for g in range(G):
-                seq.append(("dn", it - 1, g))
+                seq.append(("dn", it - lag, g))
+    return seq
+
+
+def cursor_sequence(n, r, G, iters, lag):
+    """The kernel's message cursor (TreeCursor) restated: after the up
+    messages of iteration it come the down messages of iteration it - lag;
+    once the ups are done, the remaining downs."""
+    root = r == 0
+    Q = iters * G * (1 if root else 2)
+    it = ph = g = 0
+    seq = []
+    for _ in range(Q):
+        seq.append(("up", it, g) if ph == 0 else ("dn", it - lag, g))
+        g += 1
+        if g < G:
+            continue
+        g = 0
+        if ph == 0 and not root and it >= lag:
+            ph = 1
+            continue
+        it += 1
+        if it >= iters:
+            it = max(it, lag)
+            ph = 1
+        else:
+            ph = 0
     return seq
 
 
@@ -45,9 +74,9 @@ def children(n, r):
     return [c for c in (2 * r + 1, 2 * r + 2) if c < n]
 
 
-def run_model(n, G, K, D, P, iters, seed):
+def run_model(n, G, K, D, P, iters, seed, lag=1):
     rnd = random.Random(seed)
-    seqs = [tree_messages(n, r, G, iters) for r in range(n)]
+    seqs = [tree_messages(n, r, G, iters, lag) for r in range(n)]
     npl = min(P, D)
     # per rank: ordinals of up / down messages received and sent
     info = []
@@ -82,11 +111,9 @@ def run_model(n, G, K, D, P, iters, seed):
     up_head = [0] * n  # published by the writer's signaller
     dn_head = [0] * n
     up_tail = [0] * n  # raised by the parent
-    dn_tail = [[0, 0] for _ in range(n)]  # raised by each child
     up_pub = [0] * n
     dn_pub = [0] * n
     up_slots = [[None] * K for _ in range(n)]
-    dn_slots = [[None] * K for _ in range(n)]
     stage = [[None] * D for _ in range(n)]
     fullx = [[0] * D for _ in range(n)]
     fullp = [[0] * D for _ in range(n)]
@@ -103,12 +130,7 @@ def run_model(n, G, K, D, P, iters, seed):
         return passes
 
     def credit_ok(r, m):
-        if "up_out" in m and m["up_out"] >= K and up_tail[r] < m["up_out"] - K + 1:
-            return False
-        if "dn_out" in m and m["dn_out"] >= K:
-            if min(dn_tail[r][: len(children(n, r))]) < m["dn_out"] - K + 1:
-                return False
-        return True
+        return not ("up_out" in m and m["up_out"] >= K and up_tail[r] < m["up_out"] - K + 1)
 
     def data_ok(r, m):
         if m["kind"] == "up":
@@ -150,11 +172,11 @@ def run_model(n, G, K, D, P, iters, seed):
                     assert sl is not None and sl[0] == m["up_in"], ("up slot", r, q, c, sl)
                     got.append(sl[1])
                 stage[r][q % D] = got
-            elif m["kind"] == "dn":
+            elif m["kind"] == "dn":  # the parent's output, once posted
                 par = (r - 1) // 2
-                sl = dn_slots[par][m["dn_in"] % K]
-                assert sl is not None and sl[0] == m["dn_in"], ("dn slot", r, q, sl)
-                stage[r][q % D] = [sl[1]]
+                key = (m["it"], m["g"])
+                assert key in out[par], ("output read before it was posted", r, q)
+                stage[r][q % D] = [(key, out[par][key])]
             else:
                 stage[r][q % D] = []
             fullp[r][q % D] += 1
@@ -175,17 +197,10 @@ def run_model(n, G, K, D, P, iters, seed):
                     up_slots[r][m["up_out"] % K] = (m["up_out"], (key, val))
                 else:
                     out[r][key] = val
-                    if kids:
-                        dn_slots[r][m["dn_out"] % K] = (m["dn_out"], (key, val))
             else:
-                par = (r - 1) // 2
-                side = 0 if r == 2 * par + 1 else 1
-                dn_tail[par][side] = max(dn_tail[par][side], m["dn_in"] + 1)
                 v = got[0]
                 assert v[0] == key, ("wrong down message", v, key)
                 out[r][key] = v[1]
-                if kids:
-                    dn_slots[r][m["dn_out"] % K] = (m["dn_out"], v)
             empty[r][q % D] += 1
             C[r] += 1
         else:
@@ -217,3 +232,22 @@ CASES = [(n, G, K, D, P) for n in (1, 2, 3, 5, 8) for G, K in ((1, 2), (2, 3), (
 def test_staged_tree_protocol(n, G, K, D, P):
     for seed in range(3):
         run_model(n, G, K, D, P, iters=3, seed=seed)
+
+
+@pytest.mark.parametrize("lag", [2, 3, 5])
+@pytest.mark.parametrize("n,G,K,D,P", [(n, G, G + 1, D, P) for n in (2, 3, 5, 8) for G in (1, 2, 4)
+                                       for D, P in ((1, 4), (2, 2), (3, 4))])
+def test_staged_tree_protocol_lag(n, G, K, D, P, lag):
+    # the broadcast trailing the reduction by several iterations: still no
+    # deadlock with K = G + 1, including fewer iterations than the lag
+    for iters in (1, 2, 4, 7):
+        run_model(n, G, K, D, P, iters=iters, seed=iters, lag=lag)
+
+
+@pytest.mark.parametrize("lag", [1, 2, 3])
+def test_cursor_matches_sequence(lag):
+    for n in (1, 2, 5, 8):
+        for r in range(n):
+            for G in (1, 3):
+                for iters in (1, 2, 3, 6):
+                    assert cursor_sequence(n, r, G, iters, lag) == tree_messages(n, r, G, iters, lag)
