@@ -283,9 +283,12 @@ static __device__ __noinline__ void ll128_pack_slow(const LLArgs& a, size_t j, i
   st_volatile(static_cast<char*>(a.wire_out) + 128 * j + 16 * li, make_uint4(w0, w1, w2, w3));
 }
 
-// One quad per warp per trip of a grid-stride loop; whole quads of an
-// aligned payload read their 120-byte line bodies with 8-byte loads (line j
-// starts at byte 120j, a multiple of 8).
+constexpr int kL128PackBatch = 8;  // quads per warp per trip, loads all in flight before the stores
+
+// kL128PackBatch quads per warp per trip of a grid-stride loop; whole quads
+// of an aligned payload read their 120-byte line bodies with 8-byte loads
+// (line j starts at byte 120j, a multiple of 8), every load of the trip
+// issued before its stores.
 __global__ void __launch_bounds__(kLLThreads) ll128_pack_kernel(const __grid_constant__ LLArgs a) {
   const size_t B = a.payload_bytes;
   const size_t lines = (B + 119) / 120;
@@ -297,12 +300,22 @@ __global__ void __launch_bounds__(kLLThreads) ll128_pack_kernel(const __grid_con
   char* wire = static_cast<char*>(a.wire_out);
   const size_t q0 = (size_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   // whole quads: no call in the loop
-  for (size_t q = q0; q < full; q += warps) {
-    const size_t j = 4 * q + (lane >> 3);
-    const size_t off = 120 * j + 16 * li;
-    const uint2 lo = ld_nc8(p + off);
-    const uint2 hi = li < 7 ? ld_nc8(p + off + 8) : make_uint2((uint32_t)a.flag, (uint32_t)(a.flag >> 32));
-    st_volatile(wire + 128 * j + 16 * li, make_uint4(lo.x, lo.y, hi.x, hi.y));
+  const uint2 flag2 = make_uint2((uint32_t)a.flag, (uint32_t)(a.flag >> 32));
+  for (size_t q = q0; q < full; q += kL128PackBatch * warps) {
+    uint2 lo[kL128PackBatch], hi[kL128PackBatch];
+#pragma unroll
+    for (int k = 0; k < kL128PackBatch; ++k) {
+      const size_t qk = q + k * warps;
+      const size_t off = 120 * (4 * qk + (lane >> 3)) + 16 * li;
+      lo[k] = qk < full ? ld_nc8(p + off) : make_uint2(0u, 0u);
+      hi[k] = qk < full && li < 7 ? ld_nc8(p + off + 8) : flag2;
+    }
+#pragma unroll
+    for (int k = 0; k < kL128PackBatch; ++k) {
+      const size_t qk = q + k * warps;
+      if (qk < full)
+        st_volatile(wire + 128 * (4 * qk + (lane >> 3)) + 16 * li, make_uint4(lo[k].x, lo[k].y, hi[k].x, hi[k].y));
+    }
   }
   // the rest (the payload's last, partial quad, or all of an unaligned one)
   for (size_t q = full + (q0 + warps - full % warps) % warps; q < quads; q += warps) {
