@@ -374,18 +374,24 @@ def run_ours(args):
                     h_res[key].copy_(d, non_blocking=True)
                 ev_out[k].record(s_out)
 
+    # the host link of a shared box stalls now and then (one copy of a step
+    # measured 55 ms instead of 9.4): three runs of the pipeline, the median
+    # one reported with all three
     e2e_steps = max(3, min(args.steps, 20))
     e2e_run(2)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0.record(s_in)
-    e2e_run(e2e_steps)
-    e1.record(s_out)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_runs = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(s_in)
+        e2e_run(e2e_steps)
+        e1.record(s_out)
+        torch.cuda.synchronize()
+        e2e_runs.append(e0.elapsed_time(e1))
+    e2e_ms = statistics.median(e2e_runs)
     st, info = rra.rra_query_status(stream)
     if st != 0:
         raise RuntimeError("device status after the end-to-end steps: %d %s" % (st, info))
@@ -442,6 +448,7 @@ def run_ours(args):
         "ops": ops,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "runs_ms": [round(x, 2) for x in e2e_runs], "of": "the median of three runs",
                 "overlap": "step k+1's inputs copy in and step k-1's results copy out while step k runs"},
         "gpu_launches": step.launches() * args.steps,
         "clocks": clk.summary(),
