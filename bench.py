@@ -90,11 +90,15 @@ def l2_copy_peak(torch):
 
 def ring_l2_bytes(n, S):
     """Bytes the L2-link ring moves through L2 per all-reduce of S bytes per
-    rank (4-byte types): inputs read once (n S), outputs written once (n S),
-    each of the n-1 reduce-scatter partials per rank written to a FIFO slot
-    and read back (2 (n-1) S over all ranks), and each of the n-1 forwarded
-    values per rank read from the sender's output ((n-1) S)."""
-    return 2 * n * S + 3 * (n - 1) * S
+    rank (4-byte types): inputs read once (n S; the first reduce-scatter
+    message is the sender's input tile, read by the receiver instead of the
+    sender), outputs written once (n S), each of the other n-2
+    reduce-scatter partials per rank written to a FIFO slot and read back
+    (2 (n-2) S over all ranks), and each of the n-1 forwarded values per rank
+    read from the sender's output ((n-1) S)."""
+    if n < 2:
+        return 2 * n * S
+    return 2 * n * S + 2 * (n - 2) * S + (n - 1) * S
 
 
 # --------------------------------------------------------------------------
@@ -170,6 +174,14 @@ def floor_bytes(op, n, S, e=4):
 
 def bus_factor(op, n):
     return 2 * (n - 1) / n if op.startswith("ar_") else (n - 1) / n
+
+
+# the kernel each bench operation launches (the ring's three operations
+# share one)
+KERNEL_OF = {"ar_ring": "ring_staged_kernel", "rs_ring": "ring_staged_kernel", "ag_ring": "ring_staged_kernel",
+             "ar_oneshot": "oneshot_kernel", "ar_twoshot": "twoshot_kernel", "rs_direct": "direct_rs_kernel",
+             "ag_direct": "direct_ag_kernel", "ll_pack": "ll_pack_kernel", "ll_unpack": "ll_unpack_kernel",
+             "ll128_pack": "ll128_pack_kernel", "ll128_unpack": "ll128_unpack_kernel"}
 
 
 class Step:
@@ -419,9 +431,14 @@ def run_ours(args):
             d["algbw"] = round(alg, 1)
             d["busbw"] = round(alg * bus_factor(name, N_RANKS), 1)
         ops[name] = d
-    # dominant kernel: the largest share of the step's device time among
-    # single-launch operations
-    dom = max((o for o in step.ops if o[2] == 1), key=lambda o: per_op[o[0]])
+    # dominant kernel: the largest share of the step's device time, summed
+    # over the operations that launch it; reported on its longest
+    # single-launch operation
+    share = {}
+    for name, _, _, _ in step.ops:
+        share[KERNEL_OF[name]] = share.get(KERNEL_OF[name], 0.0) + per_op[name]
+    dom_kernel = max(share, key=share.get)
+    dom = max((o for o in step.ops if KERNEL_OF[o[0]] == dom_kernel and o[2] == 1), key=lambda o: per_op[o[0]])
     dom_name, dom_bytes = dom[0], dom[1]
     achieved = dom_bytes / (per_op[dom_name] / 1e3) / 1e9
     traffic = load_traffic(dom_name)
@@ -442,7 +459,9 @@ def run_ours(args):
                    "ll_payload_bytes": step.llb, "ll_sources": LL_SRC,
                    "l2": "inputs larger than L2 (800 MB per AR op, 1 GiB LL payload); no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "op": dom_name,
+                     "share": round(share[dom_kernel] / sum(per_op[o[0]] for o in step.ops), 3),
+                     "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "traffic": traffic, "l2": l2_extra},
         "ops": ops,

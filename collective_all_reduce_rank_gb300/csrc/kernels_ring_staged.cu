@@ -37,9 +37,16 @@
 // the element type (the finished chunk, and every all-gather forward) is
 // not copied into a slot: the sender stores it in its own output, kept in
 // L2, and posts it, and the receiver bulk-copies it from there (an output is
-// never rewritten within a call, so these messages need no credit).  That
-// halves the slot writes, and L2 bandwidth is what bounds this ring.  Only
-// the inputs are read from HBM and only the outputs written to it.  Every
+// never rewritten within a call, so these messages need no credit).  The
+// first reduce-scatter message is no partial at all, only the sender's own
+// input tile: the receiver bulk-copies it from the sender's input at its
+// step 1, with no wait, and the sender skips step 0.  So of the 2(n-1)
+// sends per rank only n-2 go through slots, and L2 bandwidth is what bounds
+// this ring.  Only the inputs are read from HBM (each once, by the sender
+// or, for the first message, by its receiver) and only the outputs written
+// to it.  Two P loaders keep the CTA at 12 warps, so that it may use up to
+// 168 registers a thread without spilling (14 warps allocate as 16 and
+// cap it at 128); at the default tiles only two or three stages fit.  Every
 // role walks the message sequence with counters (no integer division on
 // the per-message path), and every mbarrier wait suspends the warp in
 // hardware rather than spinning, so waiting roles leave the issue slots to
@@ -53,31 +60,42 @@
 
 namespace rra {
 
-constexpr int kStagedPLoaders = 4;
+constexpr int kStagedPLoaders = 2;
 constexpr int kStagedConsumers = 8;
 constexpr int kStagedSignaller = 1 + kStagedPLoaders;  // warp index
 constexpr int kStagedFirstConsumer = kStagedSignaller + 1;
 constexpr int kStagedThreads = (kStagedFirstConsumer + kStagedConsumers) * 32;
 constexpr int kStagedMaxStages = 8;
 
-// Position in the message sequence: iteration, step within it, slice g.
+// Position in the message sequence: iteration, step within it (from
+// `first`, see staged_first_step), slice g.
 struct StagedCursor {
-  uint32_t it = 0, step = 0, g = 0;
+  uint32_t it = 0, step, g = 0, first;
+  __device__ __forceinline__ explicit StagedCursor(uint32_t first_) : step(first_), first(first_) {}
   __device__ __forceinline__ void next(int G, int steps) {
     if (++g == (uint32_t)G) {
       g = 0;
       if (++step == (uint32_t)steps) {
-        step = 0;
+        step = first;
         ++it;
       }
     }
   }
 };
 
+// The first reduce-scatter step only forwards the sender's own input: its
+// receiver reads that tile from the sender's input buffer at the next step
+// (a "pulled" message that needs no wait), so a rank's sequence starts at
+// step 1 whenever there is a reduce-scatter with two ranks or more.
+__host__ __device__ __forceinline__ int staged_first_step(int mode, int n) {
+  return mode != kRingAllGather && n >= 2 ? 1 : 0;
+}
+
 struct StagedMsg {
   int c;           // chunk
   bool x;          // reads the rank's own input tile
   bool in;         // receives a message (pulled from the sender's output when !x)
+  bool pin;        // the incoming message is the sender's input tile (step 1)
   bool send;       // sends a message (posted in its own output when store)
   bool store;      // writes the output
   int nw;          // 16-byte words per unit in the incoming message
@@ -94,21 +112,24 @@ __device__ __forceinline__ StagedMsg staged_msg(const RingArgs& a, int r, int ch
   StagedMsg m;
   m.base = (((size_t)k.it * a.channels + ch) * a.G + k.g) * (size_t)a.slice_units;
   int c;
+  m.pin = false;
   if (a.mode != kRingAllGather) {
-    if (step < n - 1) {  // reduce-scatter step s = step
+    if (step < n - 1) {  // reduce-scatter step s = step (>= 1: step 0 is pulled)
       c = r - step - 1;
       m.x = true;
       m.in = step > 0;
+      m.pin = step == 1;
       m.send = true;
       m.store = false;
-      m.nw = AW;
+      m.nw = step == 1 ? 1 : AW;
     } else if (step == n - 1) {  // last reduce-scatter step: chunk r complete
       c = r;
       m.x = true;
       m.in = n > 1;
+      m.pin = n == 2;
       m.send = a.mode == kRingAllReduce && n > 1;
       m.store = true;
-      m.nw = AW;
+      m.nw = n == 2 ? 1 : AW;
     } else {  // all-gather step s
       const int s = step - (n - 1);
       c = r - s;
@@ -156,9 +177,33 @@ constexpr int kStagedNT = kStagedConsumers * 32;
 
 // reduce-scatter step: partial (+ incoming partial) -> outgoing slot, as
 // accumulator words
+// The incoming message of unit u: accumulator words (a partial from a
+// slot), or the element type (the sender's input tile, `pin`).  For 4-byte
+// types the two are the same bits, so only bfloat16 tells them apart.
+template <int DT>
+__device__ __forceinline__ void staged_load_in(const unsigned char* ps, uint32_t u, bool pin, uint4* w) {
+  constexpr int AW = Elem<DT>::kAccWords;
+  if (AW == 2 && pin) {
+    w[0] = lds128(ps + (size_t)u * 16);
+  } else {
+#pragma unroll
+    for (int q = 0; q < AW; ++q) w[q] = lds128(ps + ((size_t)u * AW + q) * 16);
+  }
+}
+
+// s = incoming (+) x, in that order
+template <int DT>
+__device__ __forceinline__ void staged_acc_in(Acc& s, const uint4* w, bool pin, uint4 x) {
+  if (Elem<DT>::kAccWords == 2 && pin)
+    acc_init<DT>(s, w[0]);  // the sender's own slice
+  else
+    acc_from_words<DT>(s, w);  // the partial so far
+  acc_add<DT>(s, x);           // then this rank's slice
+}
+
 template <int DT>
 __device__ __forceinline__ void staged_partial(const unsigned char* xs, const unsigned char* ps, char* so,
-                                               uint32_t u0, uint32_t units, bool in) {
+                                               uint32_t u0, uint32_t units, bool in, bool pin) {
   constexpr int AW = Elem<DT>::kAccWords;
   constexpr int B = staged_batch<DT>();
   uint4 xv[B], pw[B][AW];
@@ -167,10 +212,7 @@ __device__ __forceinline__ void staged_partial(const unsigned char* xs, const un
     const uint32_t u = u0 + k * kStagedNT;
     if (u < units) {
       xv[k] = lds128(xs + (size_t)u * 16);
-      if (in) {
-#pragma unroll
-        for (int q = 0; q < AW; ++q) pw[k][q] = lds128(ps + ((size_t)u * AW + q) * 16);
-      }
+      if (in) staged_load_in<DT>(ps, u, pin, pw[k]);
     }
   }
 #pragma unroll
@@ -178,12 +220,10 @@ __device__ __forceinline__ void staged_partial(const unsigned char* xs, const un
     const uint32_t u = u0 + k * kStagedNT;
     if (u < units) {
       Acc s;
-      if (in) {
-        acc_from_words<DT>(s, pw[k]);  // partial so far, then this rank's slice
-        acc_add<DT>(s, xv[k]);
-      } else {
+      if (in)
+        staged_acc_in<DT>(s, pw[k], pin, xv[k]);
+      else
         acc_init<DT>(s, xv[k]);
-      }
       uint4 o[2];
       acc_to_words<DT>(s, o);
 #pragma unroll
@@ -196,7 +236,8 @@ __device__ __forceinline__ void staged_partial(const unsigned char* xs, const un
 // the element type -> output (posted to the successor when sending)
 template <int DT>
 __device__ __forceinline__ void staged_final(const unsigned char* xs, const unsigned char* ps, char* yg,
-                                             size_t base, uint32_t u0, uint32_t units, bool in, bool send) {
+                                             size_t base, uint32_t u0, uint32_t units, bool in, bool pin,
+                                             bool send) {
   constexpr int AW = Elem<DT>::kAccWords;
   constexpr int B = staged_batch<DT>();
   uint4 xv[B], pw[B][AW];
@@ -205,10 +246,7 @@ __device__ __forceinline__ void staged_final(const unsigned char* xs, const unsi
     const uint32_t u = u0 + k * kStagedNT;
     if (u < units) {
       xv[k] = lds128(xs + (size_t)u * 16);
-      if (in) {
-#pragma unroll
-        for (int q = 0; q < AW; ++q) pw[k][q] = lds128(ps + ((size_t)u * AW + q) * 16);
-      }
+      if (in) staged_load_in<DT>(ps, u, pin, pw[k]);
     }
   }
 #pragma unroll
@@ -216,12 +254,10 @@ __device__ __forceinline__ void staged_final(const unsigned char* xs, const unsi
     const uint32_t u = u0 + k * kStagedNT;
     if (u < units) {
       Acc s;
-      if (in) {
-        acc_from_words<DT>(s, pw[k]);
-        acc_add<DT>(s, xv[k]);
-      } else {
+      if (in)
+        staged_acc_in<DT>(s, pw[k], pin, xv[k]);
+      else
         acc_init<DT>(s, xv[k]);
-      }
       const uint4 val = acc_narrow<DT>(s);
       // a posted value stays in L2 for the successor's read
       if (send)
@@ -260,8 +296,8 @@ __device__ __forceinline__ void staged_forward(const unsigned char* ps, char* yg
 // thread at a time, element-wise where the unit is partial.
 template <int DT>
 __device__ __forceinline__ void staged_ragged(const StagedMsg& m, const unsigned char* xs, const unsigned char* ps,
-                                              char* so, const char* xg, const char* pg, char* yg, size_t len,
-                                              int tid) {
+                                              char* so, const char* xg, const char* pg, const char* pxg, char* yg,
+                                              size_t len, int tid) {
   constexpr int AW = Elem<DT>::kAccWords;
   for (uint32_t u = tid; u < m.units; u += kStagedNT) {
     const size_t gu = m.base + u;
@@ -278,12 +314,15 @@ __device__ __forceinline__ void staged_ragged(const StagedMsg& m, const unsigned
     }
     const uint4 xv = u < m.xfull ? lds128(xs + (size_t)u * 16) : ld_partial<DT>(xg + gu * 16, v);
     Acc s;
-    if (m.in) {
+    if (m.pin) {
+      // the sender's input tile (its partial last unit read directly)
+      const uint4 w = u < m.xfull ? lds128(ps + (size_t)u * 16) : ld_partial<DT>(pxg + gu * 16, v);
+      staged_acc_in<DT>(s, &w, true, xv);
+    } else if (m.in) {
       uint4 w[2];
       w[0] = lds128(ps + (size_t)u * 16 * AW);
       if (AW == 2) w[1] = lds128(ps + (size_t)u * 16 * AW + 16);
-      acc_from_words<DT>(s, w);
-      acc_add<DT>(s, xv);
+      staged_acc_in<DT>(s, w, false, xv);
     } else {
       acc_init<DT>(s, xv);
     }
@@ -340,9 +379,11 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
     maxu = u > maxu ? u : maxu;
   }
   const int steps = a.mode == kRingAllReduce ? 2 * n - 1 : n;
+  const uint32_t first = (uint32_t)staged_first_step(a.mode, n);
   const size_t per_iter_units = (size_t)C * G * T;
   // messages per CTA (the host keeps this below 2^31)
-  const uint32_t Q = (uint32_t)((maxu + per_iter_units - 1) / per_iter_units) * (uint32_t)(steps * G);
+  const uint32_t Q =
+      (uint32_t)((maxu + per_iter_units - 1) / per_iter_units) * (uint32_t)((steps - (int)first) * G);
 
   const int prev = (r + n - 1) % n, next = (r + 1) % n;
   const size_t link_in = (size_t)prev * C + ch, link_out = (size_t)r * C + ch;
@@ -361,7 +402,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
     const uint32_t mine = px ? 0u : (uint32_t)(warp - 1);  // P loader: messages q = mine mod np
     uint32_t pos = 0;                                       // q mod np
     uint64_t* full = px ? sh.fullx : sh.fullp;
-    StagedCursor k;
+    StagedCursor k(first);
     StagedStage st;
     // m_in: messages received (head counter); s_in / s_out: partials
     // received / sent through slots (slot index, credits)
@@ -371,9 +412,10 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
     if (mine >= np) q = Q;  // idle P loader
     for (; q < Q; ++q, k.next(G, steps), st.next(D), pos = pos + 1 == np ? 0u : pos + 1) {
       const StagedMsg m = staged_msg<DT>(a, r, ch, k);
-      const bool slot_recv = m.in && m.x, slot_send = m.send && !m.store;
+      const bool posted = m.in && !m.pin;  // counted on the head counter
+      const bool slot_recv = posted && m.x, slot_send = m.send && !m.store;
       if (!px && pos != mine) {  // another P loader's message: only count it
-        if (m.in) ++m_in;
+        if (posted) ++m_in;
         if (slot_recv) {
           ++s_in;
           if (++slot_in == (uint32_t)K) slot_in = 0;
@@ -388,7 +430,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
       }
       if (!px) {
         // incoming message posted, and a free outgoing slot, side by side
-        if (ok && m.in && lane == 0) {
+        if (ok && posted && lane == 0) {
           const uint64_t want = E | (uint64_t)(m_in + 1);
           if (seen_head < want) ok = wait_geq(head_in, want, &seen_head, a.wait, tag, r, prev, (int)q);
         }
@@ -407,19 +449,23 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
             bulk_load_stream(xbuf + (size_t)st.b * xstage,
                              static_cast<const char*>(a.in[r]) + (a.ibase[m.c] + m.base * PU) * ES, bytes, &full[st.b]);
         } else {
-          // a partial from the slot, or a value (whole units) from the
-          // sender's output
+          // a partial from the slot, or whole units of the sender's output
+          // (a value) or of its input (the first partial)
           const uint32_t bytes = !m.in ? 0u : (slot_recv ? m.units * 16u * (uint32_t)m.nw : m.xfull * 16u);
-          if (bytes) fence_proxy_async_global();  // generic-proxy writes acquired above, read by the async proxy
+          if (bytes && posted) fence_proxy_async_global();  // generic-proxy writes acquired above, read by the async proxy
           c_mbar_arrive_tx(&full[st.b], bytes);
           if (bytes && slot_recv)
             c_bulk_load(pbuf + (size_t)st.b * pstage, fifo_in + (size_t)slot_in * a.slot_bytes, bytes, &full[st.b]);
+          else if (bytes && m.pin)
+            bulk_load_stream(pbuf + (size_t)st.b * pstage,
+                             static_cast<const char*>(a.in[prev]) + (a.ibase[m.c] + m.base * PU) * ES, bytes,
+                             &full[st.b]);
           else if (bytes)
             c_bulk_load(pbuf + (size_t)st.b * pstage,
                         static_cast<const char*>(a.out[prev]) + (a.obase[m.c] + m.base * PU) * ES, bytes, &full[st.b]);
         }
       }
-      if (m.in) ++m_in;
+      if (posted) ++m_in;
       if (slot_recv) {
         ++s_in;
         if (++slot_in == (uint32_t)K) slot_in = 0;
@@ -437,7 +483,7 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
     }
   } else if (active && warp == kStagedSignaller) {
     // ---------------- signaller ----------------
-    StagedCursor k;
+    StagedCursor k(first);
     uint32_t q = 0;  // messages published
     uint32_t m_out = 0;
     uint64_t t0 = 0;
@@ -476,12 +522,12 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
     // ---------------- consumers ----------------
     const int cw = warp - kStagedFirstConsumer;
     const int tid = cw * 32 + lane;
-    StagedCursor k;
+    StagedCursor k(first);
     StagedStage st;
     uint32_t s_in = 0, slot_out = 0;  // partials received; next outgoing slot
     for (uint32_t q = 0; q < Q; ++q, k.next(G, steps), st.next(D)) {
       const StagedMsg m = staged_msg<DT>(a, r, ch, k);
-      const bool slot_recv = m.in && m.x, slot_send = m.send && !m.store;
+      const bool slot_recv = m.in && !m.pin && m.x, slot_send = m.send && !m.store;
       int ok = 1;
       if (lane == 0 && !(staged_mbar_wait(&sh.fullx[st.b], st.ph, abort, a.wait.timeout_ns) &&
                          staged_mbar_wait(&sh.fullp[st.b], st.ph, abort, a.wait.timeout_ns))) {
@@ -508,13 +554,14 @@ __global__ void __launch_bounds__(kStagedThreads, 1) ring_staged_kernel(const __
           if (!m.x)
             staged_forward<DT>(ps, yg, m.base, u0, m.units, m.send);
           else if (!m.store)
-            staged_partial<DT>(xs, ps, so, u0, m.units, m.in);
+            staged_partial<DT>(xs, ps, so, u0, m.units, m.in, m.pin);
           else
-            staged_final<DT>(xs, ps, yg, m.base, u0, m.units, m.in, m.send);
+            staged_final<DT>(xs, ps, yg, m.base, u0, m.units, m.in, m.pin, m.send);
         }
       } else {
         staged_ragged<DT>(m, xs, ps, so, static_cast<const char*>(a.in[r]) + a.ibase[m.c] * ES,
-                          static_cast<const char*>(a.out[prev]) + a.obase[m.c] * ES, yg, a.len[m.c], tid);
+                          static_cast<const char*>(a.out[prev]) + a.obase[m.c] * ES,
+                          static_cast<const char*>(a.in[prev]) + a.ibase[m.c] * ES, yg, a.len[m.c], tid);
       }
       __syncwarp();
       if (lane == 0) {

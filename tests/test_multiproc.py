@@ -65,21 +65,26 @@ def test_floor_bytes_and_bus_factors():
     assert bench.bus_factor("rs_x", 8) == model.bus_factor("reducescatter", 8)
     assert bench.bus_factor("ag_x", 8) == model.bus_factor("allgather", 8)
     # the ring's L2 bytes: inputs and outputs once, each reduce-scatter send
-    # through a slot (written, read back), each forwarded value read once from
-    # the sender's output -- 37 S at n = 8 for 4-byte types
-    assert bench.ring_l2_bytes(8, S) == 37 * S
-    assert bench.ring_l2_bytes(2, S) == 7 * S
+    # after the first through a slot (written, read back; the first is the
+    # sender's input, read once as part of the inputs), each forwarded value
+    # read once from the sender's output -- 35 S at n = 8 for 4-byte types
+    assert bench.ring_l2_bytes(8, S) == 35 * S
+    assert bench.ring_l2_bytes(2, S) == 5 * S
+    assert bench.ring_l2_bytes(1, S) == 2 * S
     # pinned to the oracle's byte counters of an actual ring all-reduce: its
-    # reduce-scatter half sends the partials, the rest are forwarded values
+    # reduce-scatter half sends n-1 partials per rank (the first of them the
+    # rank's own input), the rest are forwarded values
     import numpy as np
     import oracle
 
-    xs = [np.full(800, k, dtype=np.int32) for k in range(8)]
+    n = 8
+    xs = [np.full(800, k, dtype=np.int32) for k in range(n)]
     _, sent, _ = oracle.allreduce("ring", xs, "int32")
     _, sent_rs, _ = oracle.reduce_scatter("ring", xs, "int32")
-    partials, values = int(np.sum(sent_rs)), int(np.sum(sent)) - int(np.sum(sent_rs))
-    assert partials == values == 7 * 800 * 4
-    assert bench.ring_l2_bytes(8, 800 * 4) == 2 * 8 * 800 * 4 + 2 * partials + values
+    rs, values = int(np.sum(sent_rs)), int(np.sum(sent)) - int(np.sum(sent_rs))
+    assert rs == values == 7 * 800 * 4
+    slot_partials = rs * (n - 2) // (n - 1)
+    assert bench.ring_l2_bytes(n, 800 * 4) == 2 * n * 800 * 4 + 2 * slot_partials + values
 
 
 def test_cpu_baseline_samples():
@@ -98,3 +103,14 @@ def test_cpu_baseline_samples():
     # the all-cores variant runs the oracle on every share and reports its threads
     r = bench.cpu_baseline_all_cores(4096, min_s=0.0, max_rounds=1)
     assert r["kind"] == "oracle" and r["cores"] >= 1 and r["value"] > 0
+
+
+def test_every_bench_op_names_its_kernel():
+    # the roofline's dominant kernel is chosen by summed share over the
+    # operations that launch it
+    import bench
+
+    names = ["ar_ring", "ar_oneshot", "ar_twoshot", "rs_ring", "rs_direct", "ag_ring", "ag_direct", "ll_pack",
+             "ll_unpack", "ll128_pack", "ll128_unpack"]
+    assert set(names) == set(bench.KERNEL_OF)
+    assert {bench.KERNEL_OF[k] for k in ("ar_ring", "rs_ring", "ag_ring")} == {"ring_staged_kernel"}

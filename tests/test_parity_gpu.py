@@ -199,6 +199,48 @@ def test_ring_staged_shapes(tile, G, K, stages, dtype, n, count, monkeypatch):
             _check(got[r], want[r], dtype, "staged n=%d r=%d rep=%d" % (n, r, rep))
 
 
+@pytest.mark.parametrize("tile,G,K,stages", [(1024, 8, 16, 8), (128, 1, 2, 1), (256, 3, 4, 2), (2048, 4, 8, 3)])
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n,rc", [(2, 4), (3, 33_336), (5, 4096 * 7), (8, 1024 * 8 * 19 + 4), (8, 375_000)])
+def test_ring_staged_rs_ag_shapes(tile, G, K, stages, dtype, n, rc, monkeypatch):
+    # the staged ring's reduce-scatter and all-gather halves over message
+    # sizes, steps, FIFO depths and pipeline depths: the all-gather's
+    # forwards and the reduce-scatter's last step are read from the
+    # sender's output, not a FIFO slot; out of place and in place (the RS
+    # output at slice r of rank r's input, the AG shard at slot r of rank
+    # r's output)
+    monkeypatch.setenv("RRA_RING_PROTO", "staged")
+    monkeypatch.setenv("RRA_RING_CLUSTER", "0")
+    for k, v in (("RRA_RING_TILE", tile), ("RRA_RING_G", G), ("RRA_RING_K", K), ("RRA_RING_STAGES", stages)):
+        monkeypatch.setenv(k, str(v))
+    import gpu_util as g
+
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, n * rc, dtype, dist, seed=rc + n + tile)
+    want, _, _ = oracle.reduce_scatter("ring", xs, dtype)
+    for inplace in (False, True):
+        ins = [g.to_dev(x, dtype) for x in xs]
+        outs = [ins[r][r * rc:(r + 1) * rc] for r in range(n)] if inplace else g.empty(n, rc, dtype)
+        rra.rra_reduce_scatter(ins, outs, rc, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_RING)
+        _status_ok()
+        for r in range(n):
+            _check(g.to_host(outs[r], dtype), want[r], dtype, "staged rs n=%d r=%d inplace=%s" % (n, r, inplace))
+    shards = [x[:rc].copy() for x in xs]
+    want, _, _ = oracle.all_gather("ring", shards, dtype)
+    for inplace in (False, True):
+        outs = g.empty(n, n * rc, dtype)
+        if inplace:
+            for r in range(n):
+                outs[r][r * rc:(r + 1) * rc].copy_(g.to_dev(shards[r], dtype))
+            ins = [outs[r][r * rc:(r + 1) * rc] for r in range(n)]
+        else:
+            ins = [g.to_dev(x, dtype) for x in shards]
+        rra.rra_all_gather(ins, outs, rc, g.CODE[dtype], rra.RRA_ALGO_RING)
+        _status_ok()
+        for r in range(n):
+            _check(g.to_host(outs[r], dtype), want[r], dtype, "staged ag n=%d r=%d inplace=%s" % (n, r, inplace))
+
+
 @pytest.mark.parametrize("cluster", ["0", "1"])
 @pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
 @pytest.mark.parametrize("n,count", [(2, 5), (3, 4099), (8, 8 * 2048 * 19 * 3 + 11), (8, 1_000_003), (7, 777_777)])

@@ -6,7 +6,10 @@ bound the sender); a value in the element type -- the finished chunk the
 last reduce-scatter step forwards, and every all-gather forward -- is not
 copied into a slot: the sender stores it in its own output and posts it,
 and the receiver reads it from there (an output is never rewritten within
-a call, so it needs no credit).  The head counter counts every message.
+a call, so it needs no credit).  The first reduce-scatter "partial" is the
+sender's own input tile: the receiver reads it from the sender's input at
+its first step, with no wait, and the sender has no step 0.  The head
+counter counts every posted message.
 
 The model has the same roles and waits as the kernel: per virtual rank an X
 loader, P loaders taking messages round-robin, in-order consumers and a
@@ -33,19 +36,21 @@ class Aliasing(Exception):
 def messages(n, mode, G, iters):
     seq = []
     steps = 2 * n - 1 if mode == "ar" else n
+    first = 1 if mode != "ag" and n >= 2 else 0  # step 0 is read from the sender's input
     for it in range(iters):
-        for step in range(steps):
+        for step in range(first, steps):
             for g in range(G):
                 if mode != "ag":
                     if step < n - 1:
-                        m = dict(kind="rs", s=step, x=True, inn=step > 0, send=True, store=False)
+                        m = dict(kind="rs", s=step, x=True, inn=step > 0, pin=step == 1, send=True, store=False)
                     elif step == n - 1:
-                        m = dict(kind="fin", x=True, inn=n > 1, send=mode == "ar" and n > 1, store=True)
+                        m = dict(kind="fin", x=True, inn=n > 1, pin=n == 2, send=mode == "ar" and n > 1,
+                                 store=True)
                     else:
                         s = step - (n - 1)
-                        m = dict(kind="ag", s=s, x=False, inn=True, send=s < n - 1, store=True)
+                        m = dict(kind="ag", s=s, x=False, inn=True, pin=False, send=s < n - 1, store=True)
                 else:
-                    m = dict(kind="agf" if step == 0 else "ag", s=step, x=step == 0, inn=step > 0,
+                    m = dict(kind="agf" if step == 0 else "ag", s=step, x=step == 0, inn=step > 0, pin=False,
                              send=step < n - 1, store=True)
                 m.update(it=it, g=g)
                 seq.append(m)
@@ -69,13 +74,14 @@ def run_model(n, mode, G, K, D, P, iters, seed, cap_loaders=True):
     srin, srout = [], []  # ordinal among slot messages (partials)
     a = b = c = d = 0
     for m in seq:
-        m["slot_in"] = m["inn"] and m["kind"] in ("rs", "fin")
+        m["posted"] = m["inn"] and not m["pin"]
+        m["slot_in"] = m["posted"] and m["kind"] in ("rs", "fin")
         m["slot_out"] = m["send"] and m["kind"] == "rs"
         rin.append(a)
         rout.append(b)
         srin.append(c)
         srout.append(d)
-        a += m["inn"]
+        a += m["posted"]
         b += m["send"]
         c += m["slot_in"]
         d += m["slot_out"]
@@ -116,7 +122,7 @@ def run_model(n, mode, G, K, D, P, iters, seed, cap_loaders=True):
                 if q >= Q or not empty_passes(r, q):
                     continue
                 m = seq[q]
-                if m["inn"] and head[(r - 1) % n] < rin[q] + 1:
+                if m["posted"] and head[(r - 1) % n] < rin[q] + 1:
                     continue
                 if m["slot_out"] and srout[q] >= K and tail[r] < srout[q] - K + 1:
                     continue
@@ -143,6 +149,9 @@ def run_model(n, mode, G, K, D, P, iters, seed, cap_loaders=True):
                 sl = slots[(r - 1) % n][srin[q] % K]
                 assert sl is not None and sl[0] == srin[q], ("slot not yet written or reused", r, q)
                 stage_p[r][q % D] = sl[1]
+            elif m["pin"]:  # the sender's input tile: there from the start
+                key = (chunk_of(m, r, n), m["it"], m["g"])
+                stage_p[r][q % D] = (key, ((r - 1) % n,))
             elif m["inn"]:  # pulled from the sender's output
                 key = (chunk_of(m, r, n), m["it"], m["g"])
                 assert key in out[(r - 1) % n], ("output read before it was posted", r, q)
