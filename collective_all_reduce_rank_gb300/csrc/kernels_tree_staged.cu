@@ -12,10 +12,13 @@
 // the same bits.  bfloat16 partials travel as float32.
 //
 // One persistent cooperative launch of n x C CTAs; CTA (r, ch) is channel ch
-// of rank r.  Per channel each non-root node owns an up FIFO (its partials,
-// read by its parent) of K slots in the workspace, with a head counter
-// (messages posted) and a tail counter (messages the parent has copied
-// out).  The totals going down need no FIFO: a node with children stores
+// of rank r.  A leaf's partial is its own input, so a leaf sends nothing
+// up: its parent bulk-copies the tile from the leaf's input once the leaf
+// has joined the call (the leaf's "joined" flag), and the leaf only
+// receives.  Per channel each inner non-root node owns an up FIFO (its
+// partials, read by its parent) of K slots in the workspace, with a head
+// counter (messages posted) and a tail counter (messages the parent has
+// copied out).  The totals going down need no FIFO: a node with children stores
 // the total in its own output, kept in L2, and posts it on its down head
 // counter; both children bulk-copy it from there (an output is written once
 // per call, so these reads need no credit).  A node's messages, per
@@ -49,10 +52,19 @@ constexpr int kTreeNT = kTreeConsumers * 32;
 // it - L), slice g.  The down messages trail by L iterations; once the ups
 // are done, the remaining downs follow.
 struct TreeCursor {
-  uint32_t it = 0, ph = 0, g = 0;
+  uint32_t it, ph, g = 0;
+  bool leaf;
+  // a leaf below the root sends nothing up (its parent reads its input):
+  // it has only down messages, of tile iterations 0, 1, ...
+  __device__ __forceinline__ TreeCursor(bool leaf_, uint32_t L)
+      : it(leaf_ ? L : 0u), ph(leaf_ ? 1u : 0u), leaf(leaf_) {}
   __device__ __forceinline__ void next(int G, uint32_t iters, bool root, uint32_t L) {
     if (++g < (uint32_t)G) return;
     g = 0;
+    if (leaf) {
+      ++it;
+      return;
+    }
     if (ph == 0 && !root && it >= L) {
       ph = 1;  // the downs of iteration it - L
       return;
@@ -110,6 +122,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
   const bool root = r == 0;
   const int parent = root ? 0 : (r - 1) / 2;
   const int nk = (2 * r + 1 < n) + (2 * r + 2 < n);           // children
+  const bool leaf = nk == 0 && !root;                         // sends nothing up
+  // a child that is a leaf: its partial is its input, read from there
+  const bool lc[2] = {2 * r + 1 < n && 4 * r + 3 >= n, 2 * r + 2 < n && 4 * r + 5 >= n};
   const size_t xstage = (size_t)T * 16, pstage = (size_t)T * 16 * AW;
   unsigned char* xbuf = smem;                                 // [D][T] units
   unsigned char* p1buf = smem + (size_t)D * xstage;           // [D][T * AW]: left child / parent
@@ -135,7 +150,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
   const size_t units = (a.count + PU - 1) / PU, whole = a.count / PU;
   const size_t per_iter_units = (size_t)C * G * T;
   const uint32_t iters = (uint32_t)((units + per_iter_units - 1) / per_iter_units);
-  const uint32_t Q = iters * (uint32_t)G * (root ? 1u : 2u);
+  const uint32_t Q = iters * (uint32_t)G * (root || leaf ? 1u : 2u);
   auto tile_of = [&](const TreeCursor& k, uint32_t* nu, uint32_t* nx) -> size_t {
     const size_t base = (((size_t)k.tile_it(L) * C + ch) * G + k.g) * (size_t)T;
     *nu = base < units ? (uint32_t)(units - base < (size_t)T ? units - base : (size_t)T) : 0u;
@@ -167,7 +182,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     const uint32_t mine = px ? 0u : (uint32_t)(warp - 1);
     uint32_t pos = 0;
     uint64_t* full = px ? sh.fullx : sh.fullp;
-    TreeCursor k;
+    TreeCursor k(leaf, L);
     StagedStage st;
     uint32_t up_in = 0, dn_in = 0, up_out = 0;
     // last value seen of each polled counter: children's up heads (0, 1),
@@ -203,9 +218,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
         uint64_t want = 0;
         int peer = -1, slot = 0;
         if (up && lane < nk) {
-          f = up_head(lane == 0 ? c1 : c2);
-          want = E | (uint64_t)(up_in + 1);
+          // an inner child posts its partial; a leaf child only has to have
+          // joined the call before its input is read
           peer = lane == 0 ? c1 : c2;
+          f = lc[lane] ? joined(peer) : up_head(peer);
+          want = E | (uint64_t)(lc[lane] ? 1u : up_in + 1);
           slot = lane;
         } else if (!up && lane == 0) {
           f = dn_head(parent);
@@ -230,19 +247,32 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
             bulk_load_stream(xbuf + (size_t)st.b * xstage, static_cast<const char*>(a.in[r]) + base * 16, bytes,
                              &full[st.b]);
         } else {
-          // partials: every unit of the tile from each child's slot; the
-          // total: the whole units from the parent's output
-          const uint32_t each = up ? nu * 16u * (uint32_t)AW : nx * 16u;
-          const uint32_t bytes = has_in ? each * (up ? (uint32_t)nk : 1u) : 0u;
+          // partials: every unit of the tile from an inner child's slot, the
+          // whole units of a leaf child's input; the total: the whole units
+          // from the parent's output
+          uint32_t each[2] = {0u, 0u};
+          if (up) {
+            for (int i = 0; i < nk; ++i) each[i] = lc[i] ? nx * 16u : nu * 16u * (uint32_t)AW;
+          } else {
+            each[0] = nx * 16u;
+          }
+          const uint32_t bytes = has_in ? each[0] + each[1] : 0u;
           if (bytes) fence_proxy_async_global();
           c_mbar_arrive_tx(&full[st.b], bytes);
           if (bytes) {
             if (up) {
               const size_t so = (size_t)(up_in % (uint32_t)K) * a.slot_bytes;
-              c_bulk_load(p1buf + (size_t)st.b * pstage, up_fifo(c1) + so, each, &full[st.b]);
-              if (nk > 1) c_bulk_load(p2buf + (size_t)st.b * pstage, up_fifo(c2) + so, each, &full[st.b]);
+              unsigned char* dst[2] = {p1buf + (size_t)st.b * pstage, p2buf + (size_t)st.b * pstage};
+              for (int i = 0; i < nk; ++i) {
+                const int c = i == 0 ? c1 : c2;
+                if (each[i] == 0u) continue;
+                if (lc[i])
+                  bulk_load_stream(dst[i], static_cast<const char*>(a.in[c]) + base * 16, each[i], &full[st.b]);
+                else
+                  c_bulk_load(dst[i], up_fifo(c) + so, each[i], &full[st.b]);
+              }
             } else {
-              c_bulk_load(p1buf + (size_t)st.b * pstage, pg + base * 16, each, &full[st.b]);
+              c_bulk_load(p1buf + (size_t)st.b * pstage, pg + base * 16, each[0], &full[st.b]);
             }
           }
         }
@@ -263,7 +293,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     }
   } else if (active && warp == kTreeSignaller) {
     // ---------------- signaller ----------------
-    TreeCursor k;
+    TreeCursor k(leaf, L);
     uint32_t q = 0, up_out = 0, dn_out = 0;
     uint64_t t0 = 0;
     uint32_t spins = 0;
@@ -307,7 +337,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     // ---------------- consumers ----------------
     const int cw = warp - kTreeFirstConsumer;
     const int tid = cw * 32 + lane;
-    TreeCursor k;
+    TreeCursor k(leaf, L);
     StagedStage st;
     uint32_t up_in = 0, up_slot = 0;
     const char* xg = static_cast<const char*>(a.in[r]);
@@ -331,10 +361,10 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
       }
       mbar_try_cta(&sh.fullx[st.b], st.ph);
       mbar_try_cta(&sh.fullp[st.b], st.ph);
-      // the children's slots copied out: credits
-      if (tid == 0 && up && nk > 0) {
-        red_max_relaxed(up_tail(c1), E | (uint64_t)(up_in + 1));
-        if (nk > 1) red_max_relaxed(up_tail(c2), E | (uint64_t)(up_in + 1));
+      // the inner children's slots copied out: credits
+      if (tid == 0 && up) {
+        if (nk > 0 && !lc[0]) red_max_relaxed(up_tail(c1), E | (uint64_t)(up_in + 1));
+        if (nk > 1 && !lc[1]) red_max_relaxed(up_tail(c2), E | (uint64_t)(up_in + 1));
       }
       const unsigned char* xs = xbuf + (size_t)st.b * xstage;
       const unsigned char* p1 = p1buf + (size_t)st.b * pstage;
@@ -355,15 +385,18 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
         }
         Acc s;
         acc_init<DT>(s, u < nx ? lds128(xs + (size_t)u * 16) : ld_partial<DT>(xg + gu * 16, v));
-        if (nk > 0) {
-          uint4 w[2];
+        // the left child's partial, then the right child's: accumulator
+        // words from an inner child, the element type from a leaf's input
+        for (int i = 0; i < nk; ++i) {
+          const unsigned char* pi = i == 0 ? p1 : p2;
+          if (lc[i]) {
+            const char* cg = static_cast<const char*>(a.in[i == 0 ? c1 : c2]);
+            acc_add<DT>(s, u < nx ? lds128(pi + (size_t)u * 16) : ld_partial<DT>(cg + gu * 16, v));
+          } else {
+            uint4 w[2];
 #pragma unroll
-          for (int qq = 0; qq < AW; ++qq) w[qq] = lds128(p1 + ((size_t)u * AW + qq) * 16);
-          acc_add_words<DT>(s, w);  // left child's partial
-          if (nk > 1) {
-#pragma unroll
-            for (int qq = 0; qq < AW; ++qq) w[qq] = lds128(p2 + ((size_t)u * AW + qq) * 16);
-            acc_add_words<DT>(s, w);  // then the right child's
+            for (int qq = 0; qq < AW; ++qq) w[qq] = lds128(pi + ((size_t)u * AW + qq) * 16);
+            acc_add_words<DT>(s, w);
           }
         }
         if (send_up) {

@@ -1,8 +1,10 @@
 """A discrete-event model of the staged tree's link protocol
 (kernels_tree_staged.cu), run on the CPU under random interleavings.
 
-Nodes are virtual ranks in heap order (parent of r is (r-1)/2).  Each
-non-root node r owns an up FIFO (its partial sums, read by its parent) of K
+Nodes are virtual ranks in heap order (parent of r is (r-1)/2).  A leaf's
+partial is its own input: it sends nothing up, and its parent reads the
+tile from the leaf's input.  Each inner non-root node r owns an up FIFO
+(its partial sums, read by its parent) of K
 slots with a head counter (messages posted by the writer's signaller) and a
 tail counter (messages the parent has copied out); the writer may reuse a
 slot once the tail has passed it.  The totals come down without a FIFO: a
@@ -32,7 +34,13 @@ class Aliasing(Exception):
     pass
 
 
+def is_leaf(n, r):
+    return r > 0 and 2 * r + 1 >= n
+
+
 def tree_messages(n, r, G, iters, lag=1):
+    if is_leaf(n, r):  # sends nothing up: only the totals coming down
+        return [("dn", it, g) for it in range(iters) for g in range(G)]
     seq = []
     for it in range(iters + lag):
         if it < iters:
@@ -48,9 +56,9 @@ def cursor_sequence(n, r, G, iters, lag):
     """The kernel's message cursor (TreeCursor) restated: after the up
     messages of iteration it come the down messages of iteration it - lag;
     once the ups are done, the remaining downs."""
-    root = r == 0
-    Q = iters * G * (1 if root else 2)
-    it = ph = g = 0
+    root, leaf = r == 0, is_leaf(n, r)
+    Q = iters * G * (1 if root or leaf else 2)
+    it, ph, g = (lag, 1, 0) if leaf else (0, 0, 0)
     seq = []
     for _ in range(Q):
         seq.append(("up", it, g) if ph == 0 else ("dn", it - lag, g))
@@ -58,6 +66,9 @@ def cursor_sequence(n, r, G, iters, lag):
         if g < G:
             continue
         g = 0
+        if leaf:
+            it += 1
+            continue
         if ph == 0 and not root and it >= lag:
             ph = 1
             continue
@@ -134,7 +145,9 @@ def run_model(n, G, K, D, P, iters, seed, lag=1):
 
     def data_ok(r, m):
         if m["kind"] == "up":
-            return all(up_head[c] >= m["up_in"] + 1 for c in children(n, r)) if m["up_in"] is not None else True
+            if m["up_in"] is None:
+                return True
+            return all(up_head[c] >= m["up_in"] + 1 for c in children(n, r) if not is_leaf(n, c))
         return dn_head[(r - 1) // 2] >= m["dn_in"] + 1
 
     while True:
@@ -168,6 +181,9 @@ def run_model(n, G, K, D, P, iters, seed, lag=1):
             if m["kind"] == "up" and m["up_in"] is not None:
                 got = []
                 for c in children(n, r):
+                    if is_leaf(n, c):  # the leaf's input tile, there from the start
+                        got.append(((m["it"], m["g"]), ("x%d" % c,)))
+                        continue
                     sl = up_slots[c][m["up_in"] % K]
                     assert sl is not None and sl[0] == m["up_in"], ("up slot", r, q, c, sl)
                     got.append(sl[1])
@@ -188,8 +204,9 @@ def run_model(n, G, K, D, P, iters, seed, lag=1):
             got = stage[r][q % D]
             kids = children(n, r)
             if m["kind"] == "up":
-                for k_, c in enumerate(kids):  # credits to the children
-                    up_tail[c] = max(up_tail[c], m["up_in"] + 1)
+                for k_, c in enumerate(kids):  # credits to the inner children
+                    if not is_leaf(n, c):
+                        up_tail[c] = max(up_tail[c], m["up_in"] + 1)
                 for v in got:
                     assert v[0] == key, ("wrong up message", v, key)
                 val = ("x%d" % r,) + tuple(v[1] for v in got)  # own, then left, then right
