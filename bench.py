@@ -184,6 +184,20 @@ KERNEL_OF = {"ar_ring": "ring_staged_kernel", "rs_ring": "ring_staged_kernel", "
              "ll128_pack": "ll128_pack_kernel", "ll128_unpack": "ll128_unpack_kernel"}
 
 
+def dominant(ops, per_op):
+    """The kernel with the largest share of the step's device time, summed
+    over the operations that launch it, reported on its longest operation
+    (floor bytes and time both cover all of that operation's launches, so
+    their ratio is the per-launch rate): (kernel, operation, floor bytes,
+    share)."""
+    share = {}
+    for name, _, _, _ in ops:
+        share[KERNEL_OF[name]] = share.get(KERNEL_OF[name], 0.0) + per_op[name]
+    kernel = max(share, key=share.get)
+    name, fb = max(((o[0], o[1]) for o in ops if KERNEL_OF[o[0]] == kernel), key=lambda o: per_op[o[0]])
+    return kernel, name, fb, share[kernel] / sum(per_op[o[0]] for o in ops)
+
+
 class Step:
     """Device buffers and the sequence of C-ABI calls of one step."""
 
@@ -431,15 +445,7 @@ def run_ours(args):
             d["algbw"] = round(alg, 1)
             d["busbw"] = round(alg * bus_factor(name, N_RANKS), 1)
         ops[name] = d
-    # dominant kernel: the largest share of the step's device time, summed
-    # over the operations that launch it; reported on its longest
-    # single-launch operation
-    share = {}
-    for name, _, _, _ in step.ops:
-        share[KERNEL_OF[name]] = share.get(KERNEL_OF[name], 0.0) + per_op[name]
-    dom_kernel = max(share, key=share.get)
-    dom = max((o for o in step.ops if KERNEL_OF[o[0]] == dom_kernel and o[2] == 1), key=lambda o: per_op[o[0]])
-    dom_name, dom_bytes = dom[0], dom[1]
+    dom_kernel, dom_name, dom_bytes, dom_share = dominant(step.ops, per_op)
     achieved = dom_bytes / (per_op[dom_name] / 1e3) / 1e9
     traffic = load_traffic(dom_name)
     l2_peak = l2_copy_peak(torch)
@@ -460,7 +466,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (800 MB per AR op, 1 GiB LL payload); no flush",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom_kernel, "op": dom_name,
-                     "share": round(share[dom_kernel] / sum(per_op[o[0]] for o in step.ops), 3),
+                     "share": round(dom_share, 3),
                      "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "traffic": traffic, "l2": l2_extra},

@@ -114,3 +114,18 @@ def test_every_bench_op_names_its_kernel():
              "ll_unpack", "ll128_pack", "ll128_unpack"]
     assert set(names) == set(bench.KERNEL_OF)
     assert {bench.KERNEL_OF[k] for k in ("ar_ring", "rs_ring", "ag_ring")} == {"ring_staged_kernel"}
+
+
+def test_dominant_kernel_sums_its_operations():
+    import bench
+
+    ops = [("ar_ring", 160, 1, 1), ("rs_ring", 90, 1, 1), ("ag_ring", 90, 1, 1), ("ll_unpack", 60, 1, None),
+           ("ll_pack", 100, 4, None)]
+    # ll_unpack is the longest single operation, but the ring's three add up
+    t = {"ar_ring": 0.36, "rs_ring": 0.21, "ag_ring": 0.18, "ll_unpack": 0.37, "ll_pack": 0.50}
+    kernel, name, fb, share = bench.dominant(ops, t)
+    assert (kernel, name, fb) == ("ring_staged_kernel", "ar_ring", 160)
+    assert abs(share - 0.75 / 1.62) < 1e-12
+    # a kernel launched four times by one operation can dominate too
+    t.update(ll_pack=2.0)
+    assert bench.dominant(ops, t)[:3] == ("ll_pack_kernel", "ll_pack", 100)
