@@ -300,7 +300,14 @@ int ring_form(size_t chunk_bytes, bool staged_ok) {
   return (long)chunk_bytes <= limit ? kFormWarpLL : kFormWarpSimple;
 }
 
-constexpr size_t kStagedSmemBudget = 200u << 10;  // dynamic shared memory for the stages
+// Dynamic shared memory for the stages of the staged ring and tree
+// (RRA_STAGED_SMEM_KB, 224 KB; a CTA may have 227 KB): at 224 KB a bfloat16
+// ring tile of 1536 units (its partials travel as float32) still gets three
+// stages, which it does not at 200.
+static size_t staged_smem_budget() {
+  static const size_t b = (size_t)std::max(16L, std::min(224L, env_long("RRA_STAGED_SMEM_KB", 224))) << 10;
+  return b;
+}
 
 // Staged ring: messages of T units, G per step, K slots per link, D stages.
 // Defaults (measured on GB300, 8 ranks x 100 MB per rank): G = 6, T up to
@@ -320,7 +327,7 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
   a.G = (int)std::max(1L, env_long("RRA_RING_G", std::min<long>(6, (long)std::max<size_t>(1, gfill))));
   const long tmax = std::max(64L, std::min(4096L, env_long("RRA_RING_TILE", aw == 2 ? 1536 : 2048)));
   auto stages_for = [&](long t) {
-    const long d = (long)(kStagedSmemBudget / ((size_t)t * 16 * (1 + aw)));
+    const long d = (long)(staged_smem_budget() / ((size_t)t * 16 * (1 + aw)));
     return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_RING_STAGES", 8)}));
   };
   int occ = 0;
@@ -380,7 +387,7 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   a.lag = (int)std::max(1L, std::min(64L, env_long("RRA_TREE_LAG", aw == 2 ? 4 : 6)));
   const long tmax = std::max(64L, std::min(4096L, env_long("RRA_TREE_TILE", aw == 2 ? 1024 : 2048)));
   auto stages_for = [&](long t) {
-    const long d = (long)(kStagedSmemBudget / ((size_t)t * 16 * (1 + 2 * aw)));
+    const long d = (long)(staged_smem_budget() / ((size_t)t * 16 * (1 + 2 * aw)));
     return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_TREE_STAGES", 8)}));
   };
   int occ = 0;
