@@ -499,8 +499,10 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   // G: 4, or fewer when 16 channels of G messages would be mostly empty
   const size_t gfill = (maxu + 16 * (size_t)a.slice_units - 1) / (16 * (size_t)a.slice_units);
   a.G = (int)std::max(1L, env_long("RRA_RING_G", std::min<long>(4, (long)std::max<size_t>(1, gfill))));
+  // LL: at least 16 slots, so a small message's 2(n-1) steps rarely wait
+  // for a credit (measured 35 us against 44 at 8 ranks x 1 KiB)
   const long kmin = proto == kProtoLL ? 2L * a.G : (long)a.G + 1;
-  a.K = (int)std::max(kmin, env_long("RRA_RING_K", 2L * a.G));
+  a.K = (int)std::max(kmin, env_long("RRA_RING_K", proto == kProtoLL ? std::max(2L * a.G, 16L) : 2L * a.G));
   const int aw = dt == RRA_BFLOAT16 ? 2 : 1;
   a.slot_bytes = (size_t)a.slice_units * aw * (proto == kProtoLL ? 32 : 16);
   int occ = 0;
