@@ -20,7 +20,8 @@ so no flush is needed between operations.
 --impl reference times the CPU oracle on a bounded sample of the same step.
 --sweep FILE writes the message-size sweep (1 KiB .. 1 GiB per rank,
 n = 2, 4, 8, int32 and bfloat16, every schedule) as JSON lines and a
-tuning table for the selector.
+tuning table for the selector; with --sweep-cold every timed call follows
+a write of twice the L2 size (cold L2), hot L2 otherwise.
 """
 from __future__ import annotations
 
@@ -808,6 +809,10 @@ def run_sweep(args):
     sizes = [s for s in inputs.SWEEP_SIZES if s <= args.sweep_max]
     tune = []
     out = open(args.sweep, "w")
+    # cold-L2 mode: a scratch buffer of twice the L2 size is rewritten
+    # before every timed call
+    l2_bytes = torch.cuda.get_device_properties(0).L2_cache_size
+    flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if args.sweep_cold else None
     for n in inputs.SWEEP_RANKS:
         for dtype in ("int32", "bfloat16"):
             code = rra.RRA_INT32 if dtype == "int32" else rra.RRA_BFLOAT16
@@ -825,7 +830,10 @@ def run_sweep(args):
                 best = None
                 for name, algo in algos:
                     call = lambda: rra.rra_allreduce(ins, outs, count, code, rra.RRA_SUM, algo, stream)
-                    us, p10, p90 = time_call(torch, call, stream, S * n)
+                    if flush is None:
+                        us, p10, p90 = time_call(torch, call, stream, S * n)
+                    else:
+                        us, p10, p90 = time_call_cold(torch, call, stream, flush, S * n)
                     fb = 2 * n * S
                     alg = S / (us / 1e6) / 1e9
                     row = {"n": n, "dtype": dtype, "bytes_per_rank": S, "algo": name, "us": round(us, 3),
@@ -834,7 +842,7 @@ def run_sweep(args):
                            "floor_bytes": fb, "GBps": round(fb / (us / 1e6) / 1e9, 1),
                            "pct_hbm_8TBps": round(100 * fb / (us / 1e6) / 1e9 / HBM_NOMINAL, 1),
                            "frac_of_measured": round(fb / (us / 1e6) / 1e9 / peak, 3),
-                           "l2_resident": 2 * n * S < 4 * (126 << 20)}
+                           "l2_resident": 2 * n * S < 4 * l2_bytes, "l2": "cold" if flush is not None else "hot"}
                     out.write(json.dumps(row) + "\n")
                     out.flush()
                     if best is None or us < best[1]:
@@ -854,6 +862,25 @@ def spread(samples):
     q = sorted(samples)
     pick = lambda f: q[min(len(q) - 1, max(0, int(round(f * (len(q) - 1)))))]
     return statistics.median(q), pick(0.1), pick(0.9)
+
+
+def time_call_cold(torch, call, stream, flush, total_bytes):
+    """(median, p10, p90) microseconds of single calls, each after a write
+    of `flush` (twice the L2 size) that evicts the call's inputs and the
+    previous call's outputs from L2; the flush is outside the events."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+    reps = 20 if total_bytes < (2 << 30) else 5
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for k, (a, b) in enumerate(evs):
+            flush.fill_(k & 0xFF)
+            a.record(stream)
+            call()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return spread([a.elapsed_time(b) * 1e3 for a, b in evs])
 
 
 def time_call(torch, call, stream, total_bytes):
@@ -941,6 +968,8 @@ def main():
     ap.add_argument("--small", action="store_true", help="add the TP-activation latency table")
     ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")
     ap.add_argument("--sweep-max", type=int, default=1 << 30)
+    ap.add_argument("--sweep-cold", action="store_true",
+                    help="flush L2 (write twice its size) before every timed call of the sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
