@@ -40,6 +40,43 @@
  *   round-to-nearest in the order the schedule fixes; bfloat16 is widened
  *   to float32, summed in float32 in that order and rounded to bfloat16
  *   (nearest, ties to even) once, when the final value is stored.
+ *
+ * Environment (read by the library; none is needed, each overrides a
+ * measured default; [AIH] "Common environment variables and debugging"
+ * describes NCCL's counterparts)
+ * ------------------------------------------------------------------------
+ *   RRA_ALGO             schedule for RRA_ALGO_AUTO: ring, one_shot,
+ *                        two_shot or tree (instead of the tuning table)
+ *   RRA_TUNING_FILE      tuning table read by rra_init (default: tune/
+ *                        gb300.txt beside the library)
+ *   RRA_TIMEOUT_NS       bound of every device wait (500 ms), unless
+ *                        rra_set_timeout_ns() sets one
+ *   RRA_MAX_CTAS         CTA budget of every kernel (0: all), unless
+ *                        rra_set_max_ctas() sets one
+ *   RRA_DEBUG            1: print each call (schedule, grid, status) and
+ *                        every CUDA error to stderr
+ *   RRA_RING_PROTO       ring links for every buffer: staged (default when
+ *                        16-byte aligned), simple or ll (per-warp forms)
+ *   RRA_RING_LL_MAX_BYTES  largest chunk the per-warp ring sends as LL
+ *                        lines (64 KiB; larger ones use Simple)
+ *   RRA_RING_CLUSTER     1: the ring on thread-block clusters
+ *   RRA_RING_TILE, RRA_RING_G, RRA_RING_K, RRA_RING_STAGES,
+ *   RRA_RING_CHANNELS    staged ring: units per message (<= 2048, 1536 for
+ *                        bfloat16), messages per step (6), FIFO slots (2G),
+ *                        shared-memory stages, CTAs per rank
+ *   RRA_STAGED_SMEM_KB   shared memory for the staged ring's and tree's
+ *                        stages (224)
+ *   RRA_TREE_TILE, RRA_TREE_G, RRA_TREE_K, RRA_TREE_LAG, RRA_TREE_STAGES,
+ *   RRA_TREE_CHANNELS    staged tree: units per message (<= 2048, 1024 for
+ *                        bfloat16), tiles per iteration (24), FIFO slots
+ *                        (G + 1), iterations the broadcast trails the
+ *                        reduction (6, 4 for bfloat16), stages, CTAs per rank
+ *   RRA_TREE_CLUSTER     1: the tree on thread-block clusters
+ *   RRA_TWOSHOT_CLUSTER  1: two-shot on thread-block clusters
+ *   RRA_TWOSHOT_CHANNELS CTAs per rank of two-shot
+ *   RRA_ONESHOT_TMA      1: one-shot with bulk copies through shared memory
+ *   RRA_ONESHOT_PER_RANK 1: one-shot reads the n inputs once per rank, as
+ *                        n GPUs would
  */
 #ifndef RRA_H
 #define RRA_H
