@@ -18,20 +18,20 @@
 // receives.  Per channel each inner non-root node owns an up FIFO (its
 // partials, read by its parent) of K slots in the workspace, with a head
 // counter (messages posted) and a tail counter (messages the parent has
-// copied out).  The totals going down need no FIFO: a node with children stores
-// the total in its own output, kept in L2, and posts it on its down head
-// counter; both children bulk-copy it from there (an output is written once
-// per call, so these reads need no credit).  A node's messages, per
-// iteration of G tiles of T units: its G up messages, then -- not at the
-// root -- the G down messages of iteration it - L, so the broadcast of one
-// iteration overlaps the reduction of the next L.  Warp roles as in the staged
-// ring: an X loader (bulk-copies the node's own input tile), P loaders
-// (acquire the heads of the incoming links and the tail of the up link,
-// then bulk-copy the children's slots or the parent's output; at most as
-// many as stages, so the stage mbarriers' parity tests stay sound),
-// consumers (add, write the up slot or the output), and a signaller (one
-// fence per run of finished messages, then the head counters).  Every wait
-// is bounded.
+// copied out).  The totals going down need no FIFO: a node with children
+// stores the total in its own output, kept in L2, and posts it on its down
+// head counter; both children bulk-copy it from there (an output is
+// written once per call, so these reads need no credit).  A node's
+// messages, per iteration of G tiles of T units: its G up messages, then
+// -- not at the root -- the G down messages of iteration it - L, so the
+// broadcast of one iteration overlaps the reduction of the next L.  Warp
+// roles as in the staged ring: an X loader (bulk-copies the node's own
+// input tile), P loaders (acquire the heads of the incoming links and the
+// tail of the up link, then bulk-copy the children's slots or inputs or
+// the parent's output; at most as many as stages, so the stage mbarriers'
+// parity tests stay sound), consumers (add, write the up slot or the
+// output), and a signaller (one fence per run of finished messages, then
+// the head counters).  Every wait is bounded.
 //
 // Needs 16-byte aligned buffers.  The last tile's partial 16-byte unit is
 // read and written element-wise by the consumers.
@@ -185,9 +185,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     TreeCursor k(leaf, L);
     StagedStage st;
     uint32_t up_in = 0, dn_in = 0, up_out = 0;
-    // last value seen of each polled counter: children's up heads (0, 1),
-    // the up link's tail (2), the parent's down head (3) -- one cache per
-    // counter, never shared between two
+    // last value seen of each polled counter: the children's up heads, or
+    // a leaf child's joined flag (0, 1), the up link's tail (2), the
+    // parent's down head (3) -- one cache per counter, never shared
     uint64_t seen[4] = {0, 0, 0, 0};
     uint32_t q = 0;
     if (mine >= np) q = Q;
