@@ -127,3 +127,21 @@ def test_selector_prior_and_tuning_table(lib, tmp_path):
     assert rra.rra_load_tuning(str(bad), check=False) == rra.RRA_ERR_INVALID_ARG
     assert rra.rra_select_algo(8, 1024, rra.RRA_FLOAT32) == rra.RRA_ALGO_RING  # old table kept
     rra.rra_load_tuning(None)
+
+
+def test_shipped_tuning_table(lib):
+    # the table made by the size sweep on a GB300 loads, covers n = 2, 4, 8
+    # for int32 and bfloat16 from 1 KiB to 1 GiB, and holds its one
+    # measured exception to one-shot
+    path = os.path.join(os.path.dirname(rra.__file__), "tune", "gb300.txt")
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    assert {(int(r[0]), r[1]) for r in rows} == {(n, d) for n in (2, 4, 8) for d in ("int32", "bfloat16")}
+    assert {int(r[2]) for r in rows} == set(range(10, 31))
+    assert rra.rra_load_tuning(path) == rra.RRA_SUCCESS
+    try:
+        assert rra.rra_select_algo(2, 1 << 30, rra.RRA_INT32) == rra.RRA_ALGO_RING
+        for n in (2, 4, 8):
+            for size in (1 << 10, 1 << 20, 1 << 26):
+                assert rra.rra_select_algo(n, size, rra.RRA_BFLOAT16) == rra.RRA_ALGO_ONE_SHOT
+    finally:
+        rra.rra_load_tuning(None)
