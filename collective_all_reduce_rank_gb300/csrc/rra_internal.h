@@ -116,9 +116,8 @@ struct RingArgs {
 };
 
 // Staged tree all-reduce (persistent, cooperative).  Per channel: up FIFO
-// of node r at link r, down FIFO at link n + r; heads [2n x channels]
-// (up, then down); tails [3n x channels] (up; down read by the left child;
-// down read by the right child).
+// of inner node r at link r; heads [2n x channels] (up, then down); tails
+// [n x channels] (up); joined flags [n x channels].
 struct StagedTreeArgs {
   const void* in[kMaxRanks];
   void* out[kMaxRanks];
