@@ -588,51 +588,74 @@ int orc_allreduce_rmsnorm(int n, size_t rows, size_t hidden, int dt, const void*
 /* ------------------------------------------------------------------------ */
 
 /* "Collective communication: NCCL's algorithms and protocols, ...",
- * section "Algorithms": tree -- reduce up the tree, then broadcast down it,
- * in O(log n) steps.  The page does not fix the tree's shape or the order a
- * node adds its inputs; the reading taken: one binary tree in heap order
- * (parent of rank r is (r-1)/2, children 2r+1 and 2r+2), and a node's
- * partial is its own data, then its left child's partial, then its right
- * child's: p_r = (x_r (+) p_{2r+1}) (+) p_{2r+2}, missing children
- * skipped.  Rank 0 holds the total; the broadcast hands it down unchanged,
- * so every rank gets the same bits.  Byte counters: each non-root rank
- * sends its partial up once and receives the result once; each parent
- * receives one partial per child and sends the result once per child. */
+ * section "Algorithms": the tree is a double binary tree -- reduce up the
+ * tree, then broadcast down it, in O(log n) steps, with large messages
+ * pipelined in chunks.  The page fixes neither the two trees' shapes, nor
+ * how the data is shared between them, nor the order a node adds its
+ * inputs.  The reading taken:
+ *   - tree 0 is the binary tree in heap order over the ranks (position p
+ *     has children 2p+1 and 2p+2 and parent (p-1)/2), rank r at position
+ *     r; tree 1 is the same tree over the ranks in reverse order, rank r at
+ *     position n-1-r.  With n even, the ranks that are inner nodes of one
+ *     tree (positions below n/2) are the leaves of the other, so no rank is
+ *     an inner node of both; with n odd, rank (n-1)/2 is a leaf of both.
+ *   - the message is split in two by the chunk plan for two parts: the
+ *     first part (elements [0, H)) is reduced and broadcast on tree 0, the
+ *     second ([H, count)) on tree 1.
+ *   - a node's partial is its own data, then the partial of its child at
+ *     position 2p+1, then that of its child at 2p+2:
+ *     p = (x (+) p_{2p+1}) (+) p_{2p+2}, missing children skipped.  The
+ *     root's total is rounded once and handed down unchanged, so every rank
+ *     gets the same bits.
+ * Byte counters: in each tree every non-root node sends its partial up once
+ * and receives the total once; each parent receives one partial per child
+ * and sends the total once per child. */
+static int tree_rank_at(int t, int n, int pos) {
+  return t == 0 ? pos : n - 1 - pos;
+}
+
 int orc_allreduce_tree(int n, size_t count, int dt, const void* const* in, void* const* out,
                        uint64_t* sent, uint64_t* recv) {
   if (n < 1 || n > 64) return ORC_EINVAL;
   size_t e = elem_size(dt);
+  size_t half[3];
+  orc_chunk_plan(2, count, dt, half);
+  /* part[p]: the partial of the node at heap position p */
   void** part = (void**)calloc((size_t)n, sizeof(void*));
   if (!part) return ORC_ENOMEM;
   int rc = ORC_OK;
-  for (int r = 0; r < n; ++r) {
-    part[r] = malloc(count * 4 + 4);
-    if (!part[r]) { rc = ORC_ENOMEM; goto done; }
+  for (int p = 0; p < n; ++p) {
+    part[p] = malloc(count * 4 + 4);
+    if (!part[p]) { rc = ORC_ENOMEM; goto done; }
   }
-  /* reduce up: children have larger indices, so descending order finishes
-   * every child before its parent */
-  for (int r = n - 1; r >= 0; --r) {
-    acc_load(dt, in[r], 0, count, part[r]);
-    for (int child = 2 * r + 1; child <= 2 * r + 2; ++child) {
-      if (child >= n) continue;
-      tally(sent, child, count * e);
-      tally(recv, r, count * e);
-      if (dt == ORC_INT32)
-        for (size_t i = 0; i < count; ++i) ((uint32_t*)part[r])[i] += ((uint32_t*)part[child])[i];
-      else
-        for (size_t i = 0; i < count; ++i) ((float*)part[r])[i] = ((float*)part[r])[i] + ((float*)part[child])[i];
+  for (int t = 0; t < 2; ++t) {
+    const size_t lo = half[t], len = half[t + 1] - half[t];
+    /* reduce up: children sit at larger positions, so descending positions
+     * finish every child before its parent */
+    for (int p = n - 1; p >= 0; --p) {
+      const int r = tree_rank_at(t, n, p);
+      acc_load(dt, in[r], lo, len, part[p]);
+      for (int child = 2 * p + 1; child <= 2 * p + 2; ++child) {
+        if (child >= n) continue;
+        tally(sent, tree_rank_at(t, n, child), len * e);
+        tally(recv, r, len * e);
+        if (dt == ORC_INT32)
+          for (size_t i = 0; i < len; ++i) ((uint32_t*)part[p])[i] += ((uint32_t*)part[child])[i];
+        else
+          for (size_t i = 0; i < len; ++i) ((float*)part[p])[i] = ((float*)part[p])[i] + ((float*)part[child])[i];
+      }
+    }
+    /* broadcast down: the root's rounded total, forwarded unchanged */
+    acc_store(dt, part[0], out[tree_rank_at(t, n, 0)], lo, len);
+    for (int p = 1; p < n; ++p) {
+      const int r = tree_rank_at(t, n, p), parent = tree_rank_at(t, n, (p - 1) / 2);
+      memcpy((char*)out[r] + lo * e, (const char*)out[parent] + lo * e, len * e);
+      tally(sent, parent, len * e);
+      tally(recv, r, len * e);
     }
   }
-  /* broadcast down: the root's rounded total, forwarded unchanged */
-  acc_store(dt, part[0], out[0], 0, count);
-  for (int r = 1; r < n; ++r) {
-    int parent = (r - 1) / 2;
-    memcpy(out[r], out[parent], count * e);
-    tally(sent, parent, count * e);
-    tally(recv, r, count * e);
-  }
 done:
-  for (int r = 0; r < n; ++r) free(part[r]);
+  for (int p = 0; p < n; ++p) free(part[p]);
   free(part);
   return rc;
 }
