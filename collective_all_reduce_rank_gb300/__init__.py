@@ -20,13 +20,15 @@ import threading
 
 from . import build as _build
 
-RRA_SUCCESS = 0
+RRA_OK = 0
+RRA_SUCCESS = RRA_OK
 RRA_ERR_INVALID_ARG = 1
 RRA_ERR_UNSUPPORTED = 2
 RRA_ERR_ALIAS = 3
 RRA_ERR_NOT_INITIALIZED = 4
 RRA_ERR_CUDA = 5
 RRA_ERR_TIMEOUT = 6
+RRA_ERR_WORKSPACE = 7
 
 RRA_INT32 = 0
 RRA_FLOAT32 = 1
@@ -85,7 +87,7 @@ def _declare(lib):
     i, sz, u32, u64 = ctypes.c_int, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint64
     sigs = {
         "rra_init": (i, [i, sz]),
-        "rra_finalize": (i, [i]),
+        "rra_finalize": (i, []),
         "rra_allreduce": (i, [vpp, vpp, i, sz, i, i, i, vp]),
         "rra_allreduce_two_shot_static": (i, [vpp, vpp, i, sz, i, i, vp]),
         "rra_reduce_scatter": (i, [vpp, vpp, i, sz, i, i, i, vp]),
@@ -98,6 +100,7 @@ def _declare(lib):
         "rra_ll128_pack": (i, [vp, sz, vp, u64, vp]),
         "rra_ll128_unpack": (i, [vpp, i, vp, sz, i, i, u64, vp]),
         "rra_query_status": (i, [vp, ctypes.POINTER(ctypes.c_int32)]),
+        "rra_query_status_static": (i, [vp, ctypes.POINTER(ctypes.c_int32)]),
         "rra_select_algo": (i, [i, sz, i]),
         "rra_load_tuning": (i, [ctypes.c_char_p]),
         "rra_set_timeout_ns": (None, [u64]),
@@ -192,8 +195,8 @@ def rra_init(device: int = 0, workspace_bytes: int = 0, check: bool = True) -> i
     return _ret(load().rra_init(device, workspace_bytes), "rra_init", check)
 
 
-def rra_finalize(device: int = 0, check: bool = True) -> int:
-    return _ret(load().rra_finalize(device), "rra_finalize", check)
+def rra_finalize(check: bool = True) -> int:
+    return _ret(load().rra_finalize(), "rra_finalize", check)
 
 
 def rra_allreduce(bufs, outs, count=None, dtype=None, op=RRA_SUM, algo=RRA_ALGO_AUTO, stream=None,
@@ -296,6 +299,15 @@ def rra_query_status(stream=None):
     Returns (status, [code, rank, peer, index])."""
     info = (ctypes.c_int32 * 4)()
     st = load().rra_query_status(_stream(stream), info)
+    return st, list(info)
+
+
+def rra_query_status_static(stream=None):
+    """Synchronize the stream and read/clear the status of
+    rra_allreduce_two_shot_static (allocates nothing).
+    Returns (status, [code, rank, peer, index])."""
+    info = (ctypes.c_int32 * 4)()
+    st = load().rra_query_status_static(_stream(stream), info)
     return st, list(info)
 
 

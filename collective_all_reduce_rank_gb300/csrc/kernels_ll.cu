@@ -1,16 +1,15 @@
 // kernels_ll.cu -- LL and LL128 wire formats: pack, and unpack fused with
 // a SUM over several sources.
 //
-// "Collective communication: NCCL's algorithms and protocols, and custom
-// all-reduce in inference frameworks", section "Protocols: how do you know
-// the data has arrived":
-//   LL    -- every 8 bytes hold 4 bytes of data and 4 bytes of flag; the
-//            receiver polls the flag; relies on 8-byte writes being atomic,
-//            so no memory fence is needed (about 50% efficiency);
-//   LL128 -- every 128 bytes hold 120 bytes of data and 8 bytes of flag
-//            (about 94% efficiency).
-// Layout used here: data first, flag last, little-endian; the payload's tail
-// is zero-padded.
+// The two formats are those of "Collective communication: NCCL's
+// algorithms and protocols, and custom all-reduce in inference frameworks",
+// section "Protocols: how do you know the data has arrived".  An LL line is
+// 8 bytes, half payload and half flag, so it carries data at half the wire
+// rate; the reader spins on the flag word, and since the 8 bytes travel in
+// one indivisible store, finding the flag means finding the data, with no
+// fence in between.  An LL128 line is 128 bytes: 120 of payload and an
+// 8-byte flag, so 15/16 of the wire is data.  Layout used here: data first,
+// flag last, little-endian; the payload's tail is zero-padded.
 //
 // LL lines are written and read as 64-bit elements (two per 16-byte vector
 // access), and an aligned 64-bit access is single-copy atomic, so a reader

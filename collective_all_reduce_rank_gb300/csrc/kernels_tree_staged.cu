@@ -1,37 +1,57 @@
-// kernels_tree_staged.cu -- tree all-reduce with whole-CTA messages staged in
-// shared memory by bulk copies, links through L2 (the machinery of the
-// staged ring, kernels_ring_staged.cu).
+// kernels_tree_staged.cu -- double binary tree all-reduce with whole-CTA
+// messages staged in shared memory by bulk copies, links through L2 (the
+// machinery of the staged ring, kernels_ring_staged.cu).
 //
 // "Collective communication: NCCL's algorithms and protocols, and custom
-// all-reduce in inference frameworks", section "Algorithms": tree -- reduce
-// up the tree, then broadcast down it, in O(log n) steps.  The tree is one
-// binary tree in heap order (parent of rank r is (r-1)/2, children 2r+1 and
-// 2r+2); a node's partial is its own data, then its left child's partial,
-// then its right child's: p_r = (x_r (+) p_{2r+1}) (+) p_{2r+2}.  The root
-// rounds the total once and it travels down unchanged, so every rank holds
-// the same bits.  bfloat16 partials travel as float32.
+// all-reduce in inference frameworks", section "Algorithms": the tree is a
+// double binary tree -- reduce up, broadcast down, O(log n) steps, large
+// messages pipelined in chunks.  Tree 0 is the binary tree in heap order
+// over the ranks (rank r at position r; position p has children 2p+1 and
+// 2p+2), tree 1 the same tree over the ranks reversed (rank r at position
+// n-1-r).  The message is split in two by the chunk plan for two parts:
+// units [0, half_units) go over tree 0, the rest over tree 1.  A node's
+// partial is its own data, then its child 2p+1's partial, then its child
+// 2p+2's: p = (x (+) p_{2p+1}) (+) p_{2p+2}.  Each root rounds its total
+// once and it travels down unchanged, so every rank holds the same bits.
+// bfloat16 partials travel as float32.
 //
-// One persistent cooperative launch of n x C CTAs; CTA (r, ch) is channel ch
-// of rank r.  A leaf's partial is its own input, so a leaf sends nothing
-// up: its parent bulk-copies the tile from the leaf's input once the leaf
-// has joined the call (the leaf's "joined" flag), and the leaf only
-// receives.  Per channel each inner non-root node owns an up FIFO (its
-// partials, read by its parent) of K slots in the workspace, with a head
-// counter (messages posted) and a tail counter (messages the parent has
-// copied out).  The totals going down need no FIFO: a node with children
-// stores the total in its own output, kept in L2, and posts it on its down
-// head counter; both children bulk-copy it from there (an output is
-// written once per call, so these reads need no credit).  A node's
-// messages, per iteration of G tiles of T units: its G up messages, then
-// -- not at the root -- the G down messages of iteration it - L, so the
-// broadcast of one iteration overlaps the reduction of the next L.  Warp
-// roles as in the staged ring: an X loader (bulk-copies the node's own
-// input tile), P loaders (acquire the heads of the incoming links and the
-// tail of the up link, then bulk-copy the children's slots or inputs or
-// the parent's output; at most as many as stages, so the stage mbarriers'
-// parity tests stay sound), consumers (add, write the up slot or the
-// output), and a signaller (one fence per run of finished messages, then
-// the head counters).  Every wait is bounded.
+// A rank has children in at most one of the two trees (with n even it is an
+// inner node of one and a leaf of the other; with n odd rank (n-1)/2 is a
+// leaf of both), so it sends partials up, and posts totals down, in at
+// most one tree: its up FIFO, up head and tail and down head are one per
+// (rank, channel), as for a single tree.
+//
+// One persistent cooperative launch of n x C CTAs; CTA (r, ch) is channel
+// ch of rank r in BOTH trees, so that every CTA carries one heavy role (the
+// tree where the rank has children) and one light one (the tree where it is
+// a leaf), and no SM idles behind a leaf's light load.  A leaf's partial is
+// its own input, so a leaf sends nothing up: its parent bulk-copies the
+// tile from the leaf's input once the leaf has joined the call (the leaf's
+// "joined" flag), and the leaf only receives.  Per channel each inner
+// non-root node owns an up FIFO (its partials, read by its parent) of K
+// slots in the workspace, with a head counter (messages posted) and a tail
+// counter (messages the parent has copied out).  The totals going down need
+// no FIFO: a node with children stores the total in its own output, kept
+// in L2, and posts it on its down head counter; both children bulk-copy it
+// from there (an output is written once per call, so these reads need no
+// credit).
+//
+// Message order.  Tiles of T units, G per iteration.  At pipeline time t a
+// CTA handles, in this order, the up messages of tile iteration t (in the
+// tree where it has children), then the down messages of tile iteration
+// t - L of tree 0, then those of tree 1 (the broadcast trails the reduction
+// by L iterations, so it overlaps the next L iterations' reduction).
+// Every cross-CTA wait is on a message of an earlier time or of the same
+// time and kind in the same tree, where up waits run from parent to child
+// and down waits from child to parent, so no chain of waits closes on
+// itself; a credit wait is on a message at least one time earlier (K >
+// G).  Warp roles as in the staged ring: an X loader (bulk-copies the
+// node's own input tile), P loaders (acquire the heads of the incoming
+// links and the tail of the up link, then bulk-copy the children's slots
+// or inputs or the parent's output; at most as many as stages, so the stage
+// mbarriers' parity tests stay sound), consumers (add, write the up slot or
+// the output), and a signaller (one fence per run of finished messages,
+// then the head counters).  Every wait is bounded.
 //
 // Needs 16-byte aligned buffers.  The last tile's partial 16-byte unit is
 // read and written element-wise by the consumers.
@@ -47,37 +67,71 @@ constexpr int kTreeThreads = (kTreeFirstConsumer + kTreeConsumers) * 32;
 constexpr int kTreeMaxStages = 8;
 constexpr int kTreeNT = kTreeConsumers * 32;
 
-// Position in a node's message sequence: iteration `it`, phase (0 = up
-// messages of tile iteration it, 1 = down messages of tile iteration
-// it - L), slice g.  The down messages trail by L iterations; once the ups
-// are done, the remaining downs follow.
+// rank at heap position `pos` of tree t
+__device__ __forceinline__ int tree_rank_at(int t, int n, int pos) { return t == 0 ? pos : n - 1 - pos; }
+
+// Rank r's place in tree t.
+struct TreeRole {
+  int parent;      // the parent's rank (the root: its own)
+  int kid[2];      // the children's ranks, position 2p+1 first (-1: none)
+  int nk;          // children
+  bool root;       // position 0
+  bool leaf;       // below the root, no children: sends nothing up
+  bool lc[2];      // child i is a leaf: its partial is its input
+};
+
+__device__ __forceinline__ TreeRole tree_role(int t, int n, int r) {
+  const int p = t == 0 ? r : n - 1 - r;
+  TreeRole o;
+  o.root = p == 0;
+  o.parent = o.root ? r : tree_rank_at(t, n, (p - 1) / 2);
+  o.nk = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int c = 2 * p + 1 + i;
+    o.kid[i] = c < n ? tree_rank_at(t, n, c) : -1;
+    o.lc[i] = c < n && 2 * c + 1 >= n;
+    o.nk += c < n ? 1 : 0;
+  }
+  o.leaf = !o.root && o.nk == 0;
+  return o;
+}
+
+// The CTA's message classes: 0 = up messages of tree 0, 1 = up messages of
+// tree 1, 2 = down messages of tree 0, 3 = down messages of tree 1; class
+// c has messages at the times [lo[c], hi[c]) (G per time).
+struct TreeSeq {
+  uint32_t lo[4], hi[4], tend;
+};
+
+// Position in the CTA's message sequence: time t, class, slice g.
 struct TreeCursor {
-  uint32_t it, ph, g = 0;
-  bool leaf;
-  // a leaf below the root sends nothing up (its parent reads its input):
-  // it has only down messages, of tile iterations 0, 1, ...
-  __device__ __forceinline__ TreeCursor(bool leaf_, uint32_t L)
-      : it(leaf_ ? L : 0u), ph(leaf_ ? 1u : 0u), leaf(leaf_) {}
-  __device__ __forceinline__ void next(int G, uint32_t iters, bool root, uint32_t L) {
-    if (++g < (uint32_t)G) return;
-    g = 0;
-    if (leaf) {
-      ++it;
-      return;
-    }
-    if (ph == 0 && !root && it >= L) {
-      ph = 1;  // the downs of iteration it - L
-      return;
-    }
-    ++it;
-    if (it >= iters) {
-      if (it < L) it = L;
-      ph = 1;
-    } else {
-      ph = 0;
+  uint32_t t = 0, cls = 0, g = 0;
+  // from (t, cls) on, the first class with messages
+  __device__ __forceinline__ void seek(const TreeSeq& s) {
+    while (t < s.tend) {
+      int found = -1;
+#pragma unroll
+      for (int c = 3; c >= 0; --c)
+        if (c >= (int)cls && s.lo[c] <= t && t < s.hi[c]) found = c;
+      if (found >= 0) {
+        cls = (uint32_t)found;
+        return;
+      }
+      cls = 0;
+      ++t;
     }
   }
-  __device__ __forceinline__ uint32_t tile_it(uint32_t L) const { return ph == 0 ? it : it - L; }
+  __device__ __forceinline__ explicit TreeCursor(const TreeSeq& s) { seek(s); }
+  __device__ __forceinline__ void next(int G, const TreeSeq& s) {
+    if (++g < (uint32_t)G) return;
+    g = 0;
+    ++cls;
+    seek(s);
+  }
+  __device__ __forceinline__ int tree() const { return (int)(cls & 1u); }
+  __device__ __forceinline__ bool up() const { return cls < 2u; }
+  __device__ __forceinline__ uint32_t tile_it(uint32_t L) const { return cls < 2u ? t : t - L; }
 };
 
 struct TreeShared {
@@ -119,16 +173,14 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
   const uint32_t L = (uint32_t)a.lag;
   const int r = blockIdx.x % n, ch = blockIdx.x / n;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool root = r == 0;
-  const int parent = root ? 0 : (r - 1) / 2;
-  const int nk = (2 * r + 1 < n) + (2 * r + 2 < n);           // children
-  const bool leaf = nk == 0 && !root;                         // sends nothing up
-  // a child that is a leaf: its partial is its input, read from there
-  const bool lc[2] = {2 * r + 1 < n && 4 * r + 3 >= n, 2 * r + 2 < n && 4 * r + 5 >= n};
+  const TreeRole R0 = tree_role(0, n, r), R1 = tree_role(1, n, r);
+  // the tree where this rank has children (its up messages); with none
+  // (n odd, the middle rank) it has down messages only
+  const TreeRole Rp = R0.nk > 0 ? R0 : R1;
   const size_t xstage = (size_t)T * 16, pstage = (size_t)T * 16 * AW;
   unsigned char* xbuf = smem;                                 // [D][T] units
-  unsigned char* p1buf = smem + (size_t)D * xstage;           // [D][T * AW]: left child / parent
-  unsigned char* p2buf = p1buf + (size_t)D * pstage;          // [D][T * AW]: right child
+  unsigned char* p1buf = smem + (size_t)D * xstage;           // [D][T * AW]: first child / parent
+  unsigned char* p2buf = p1buf + (size_t)D * pstage;          // [D][T * AW]: second child
 
   if (threadIdx.x == 0) {
     sh.epoch = read_epoch(a.wait.sync);
@@ -147,14 +199,31 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
   const uint32_t tag = epoch + 1u;
   volatile uint32_t* abort = &sh.abort;
 
+  // the two parts of the message, in units
   const size_t units = (a.count + PU - 1) / PU, whole = a.count / PU;
+  const size_t ulo[2] = {0, a.half_units}, uhi[2] = {a.half_units, units};
   const size_t per_iter_units = (size_t)C * G * T;
-  const uint32_t iters = (uint32_t)((units + per_iter_units - 1) / per_iter_units);
-  const uint32_t Q = iters * (uint32_t)G * (root || leaf ? 1u : 2u);
+  TreeSeq seq;
+  uint32_t Q = 0;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const TreeRole& R = t == 0 ? R0 : R1;
+    const uint32_t iters = (uint32_t)((uhi[t] - ulo[t] + per_iter_units - 1) / per_iter_units);
+    seq.lo[t] = 0;
+    seq.hi[t] = R.leaf ? 0u : iters;
+    seq.lo[2 + t] = L;
+    seq.hi[2 + t] = R.root ? L : L + iters;
+    Q += (seq.hi[t] - seq.lo[t] + seq.hi[2 + t] - seq.lo[2 + t]) * (uint32_t)G;
+  }
+  seq.tend = 0;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) seq.tend = seq.hi[c] > seq.tend ? seq.hi[c] : seq.tend;
   auto tile_of = [&](const TreeCursor& k, uint32_t* nu, uint32_t* nx) -> size_t {
-    const size_t base = (((size_t)k.tile_it(L) * C + ch) * G + k.g) * (size_t)T;
-    *nu = base < units ? (uint32_t)(units - base < (size_t)T ? units - base : (size_t)T) : 0u;
-    *nx = base < whole ? (uint32_t)(whole - base < (size_t)T ? whole - base : (size_t)T) : 0u;
+    const int t = k.tree();
+    const size_t hi = t ? uhi[1] : uhi[0];
+    const size_t base = (t ? ulo[1] : ulo[0]) + (((size_t)k.tile_it(L) * C + ch) * G + k.g) * (size_t)T;
+    *nu = base < hi ? (uint32_t)(hi - base < (size_t)T ? hi - base : (size_t)T) : 0u;
+    *nx = base < whole ? (uint32_t)(whole - base < (size_t)*nu ? whole - base : (size_t)*nu) : 0u;
     return base;
   };
 
@@ -164,9 +233,6 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
   auto up_head = [&](int node) { return a.head + (size_t)node * C + ch; };
   auto dn_head = [&](int node) { return a.head + (size_t)(n + node) * C + ch; };
   auto up_tail = [&](int node) { return a.tail + (size_t)node * C + ch; };
-  // the parent's output: the totals coming down
-  const char* pg = static_cast<const char*>(a.out[parent]);
-  const int c1 = 2 * r + 1, c2 = 2 * r + 2;
   const bool active = r != a.wait.skip_rank;
   // joined flags: each CTA marks its (rank, channel) for this call before
   // any wait, so an expired wait can tell a rank that never took part from
@@ -182,27 +248,28 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     const uint32_t mine = px ? 0u : (uint32_t)(warp - 1);
     uint32_t pos = 0;
     uint64_t* full = px ? sh.fullx : sh.fullp;
-    TreeCursor k(leaf, L);
+    TreeCursor k(seq);
     StagedStage st;
-    uint32_t up_in = 0, dn_in = 0, up_out = 0;
+    uint32_t up_in = 0, up_out = 0, dn_in0 = 0, dn_in1 = 0;  // down messages received per tree
     // last value seen of each polled counter: the children's up heads, or
     // a leaf child's joined flag (0, 1), the up link's tail (2), the
-    // parent's down head (3) -- one cache per counter, never shared
-    uint64_t seen[4] = {0, 0, 0, 0};
+    // parents' down heads in tree 0 and tree 1 (3, 4) -- one cache per
+    // counter, never shared
+    uint64_t seen[5] = {0, 0, 0, 0, 0};
     uint32_t q = 0;
     if (mine >= np) q = Q;
-    for (; q < Q; ++q, k.next(G, iters, root, L), st.next(D), pos = pos + 1 == np ? 0u : pos + 1) {
-      const bool up = k.ph == 0;
+    for (; q < Q; ++q, k.next(G, seq), st.next(D), pos = pos + 1 == np ? 0u : pos + 1) {
+      const bool up = k.up();
+      const int tr = k.tree();
       uint32_t nu, nx;
       const size_t base = tile_of(k, &nu, &nx);
-      const bool has_in = up ? nk > 0 : true;
-      const bool send_up = up && !root;
+      const bool send_up = up && !Rp.root;
       if (!px && pos != mine) {  // another P loader's message: only count it
         if (up) {
-          if (nk > 0) ++up_in;
+          ++up_in;
           if (send_up) ++up_out;
         } else {
-          ++dn_in;
+          ++(tr ? dn_in1 : dn_in0);
         }
         continue;
       }
@@ -211,28 +278,30 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
         if (!*abort) record_error(a.wait.status, RRA_ERR_TIMEOUT, r, -1, (int)q, tag);
         ok = 0;
       }
+      const int parent = tr ? R1.parent : R0.parent;
       if (!px && ok) {
         // lanes 0/1: incoming heads (children, or the parent); lane 2: the
         // up link's tail; side by side
         const uint64_t* f = nullptr;
         uint64_t want = 0;
         int peer = -1, slot = 0;
-        if (up && lane < nk) {
+        if (up && lane < Rp.nk) {
           // an inner child posts its partial; a leaf child only has to have
           // joined the call before its input is read
-          peer = lane == 0 ? c1 : c2;
-          f = lc[lane] ? joined(peer) : up_head(peer);
-          want = E | (uint64_t)(lc[lane] ? 1u : up_in + 1);
+          const bool leaf_kid = lane == 0 ? Rp.lc[0] : Rp.lc[1];
+          peer = lane == 0 ? Rp.kid[0] : Rp.kid[1];
+          f = leaf_kid ? joined(peer) : up_head(peer);
+          want = E | (uint64_t)(leaf_kid ? 1u : up_in + 1);
           slot = lane;
         } else if (!up && lane == 0) {
           f = dn_head(parent);
-          want = E | (uint64_t)(dn_in + 1);
+          want = E | (uint64_t)((tr ? dn_in1 : dn_in0) + 1);
           peer = parent;
-          slot = 3;
+          slot = 3 + tr;
         } else if (lane == 2 && send_up && up_out >= (uint32_t)K) {
           f = up_tail(r);
           want = E | (uint64_t)(up_out - K + 1);
-          peer = parent;
+          peer = Rp.parent;
           slot = 2;
         }
         if (f && seen[slot] < want) ok = wait_geq(f, want, &seen[slot], a.wait, tag, r, peer, (int)q, joined(peer));
@@ -252,36 +321,40 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
           // from the parent's output
           uint32_t each[2] = {0u, 0u};
           if (up) {
-            for (int i = 0; i < nk; ++i) each[i] = lc[i] ? nx * 16u : nu * 16u * (uint32_t)AW;
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              if (i < Rp.nk) each[i] = Rp.lc[i] ? nx * 16u : nu * 16u * (uint32_t)AW;
           } else {
             each[0] = nx * 16u;
           }
-          const uint32_t bytes = has_in ? each[0] + each[1] : 0u;
+          const uint32_t bytes = each[0] + each[1];
           if (bytes) fence_proxy_async_global();
           c_mbar_arrive_tx(&full[st.b], bytes);
           if (bytes) {
             if (up) {
               const size_t so = (size_t)(up_in % (uint32_t)K) * a.slot_bytes;
               unsigned char* dst[2] = {p1buf + (size_t)st.b * pstage, p2buf + (size_t)st.b * pstage};
-              for (int i = 0; i < nk; ++i) {
-                const int c = i == 0 ? c1 : c2;
-                if (each[i] == 0u) continue;
-                if (lc[i])
+#pragma unroll
+              for (int i = 0; i < 2; ++i) {
+                const int c = Rp.kid[i];
+                if (i >= Rp.nk || each[i] == 0u) continue;
+                if (Rp.lc[i])
                   bulk_load_stream(dst[i], static_cast<const char*>(a.in[c]) + base * 16, each[i], &full[st.b]);
                 else
                   c_bulk_load(dst[i], up_fifo(c) + so, each[i], &full[st.b]);
               }
             } else {
-              c_bulk_load(p1buf + (size_t)st.b * pstage, pg + base * 16, each[0], &full[st.b]);
+              c_bulk_load(p1buf + (size_t)st.b * pstage, static_cast<const char*>(a.out[parent]) + base * 16,
+                          each[0], &full[st.b]);
             }
           }
         }
       }
       if (up) {
-        if (nk > 0) ++up_in;
+        ++up_in;
         if (send_up) ++up_out;
       } else {
-        ++dn_in;
+        ++(tr ? dn_in1 : dn_in0);
       }
     }
     if (q < Q && lane == 0) {
@@ -293,7 +366,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     }
   } else if (active && warp == kTreeSignaller) {
     // ---------------- signaller ----------------
-    TreeCursor k(leaf, L);
+    TreeCursor k(seq);
     uint32_t q = 0, up_out = 0, dn_out = 0;
     uint64_t t0 = 0;
     uint32_t spins = 0;
@@ -304,10 +377,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
       for (int o = 16; o > 0; o >>= 1) d = min(d, __shfl_xor_sync(0xffffffffu, d, o));
       if (d > q) {
         uint32_t nup = 0, ndn = 0;
-        for (; q < d; ++q, k.next(G, iters, root, L)) {
-          const bool up = k.ph == 0;
-          if (up && !root) ++nup;
-          if (up ? (root && nk > 0) : nk > 0) ++ndn;
+        for (; q < d; ++q, k.next(G, seq)) {
+          if (k.up()) {
+            if (!Rp.root) ++nup;
+            else if (Rp.nk > 0) ++ndn;  // a root posts its totals
+          } else if ((k.tree() ? R1.nk : R0.nk) > 0) {
+            ++ndn;
+          }
         }
         if ((nup || ndn) && lane == 0) {
           fence_acq_rel();
@@ -337,17 +413,20 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
     // ---------------- consumers ----------------
     const int cw = warp - kTreeFirstConsumer;
     const int tid = cw * 32 + lane;
-    TreeCursor k(leaf, L);
+    TreeCursor k(seq);
     StagedStage st;
     uint32_t up_in = 0, up_slot = 0;
     const char* xg = static_cast<const char*>(a.in[r]);
     char* yg = static_cast<char*>(a.out[r]);
-    for (uint32_t q = 0; q < Q; ++q, k.next(G, iters, root, L), st.next(D)) {
-      const bool up = k.ph == 0;
+    for (uint32_t q = 0; q < Q; ++q, k.next(G, seq), st.next(D)) {
+      const bool up = k.up();
+      const int tr = k.tree();
       uint32_t nu, nx;
       const size_t base = tile_of(k, &nu, &nx);
-      const bool send_up = up && !root;
-      const bool send_dn = up ? (root && nk > 0) : nk > 0;
+      const bool send_up = up && !Rp.root;
+      // a node with children keeps the total it stores in L2 for them
+      const bool send_dn = up ? (Rp.root && Rp.nk > 0) : (tr ? R1.nk : R0.nk) > 0;
+      const char* pg = static_cast<const char*>(a.out[tr ? R1.parent : R0.parent]);
       int ok = 1;
       if (lane == 0 && !(staged_mbar_wait(&sh.fullx[st.b], st.ph, abort, a.wait.timeout_ns) &&
                          staged_mbar_wait(&sh.fullp[st.b], st.ph, abort, a.wait.timeout_ns))) {
@@ -363,8 +442,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
       mbar_try_cta(&sh.fullp[st.b], st.ph);
       // the inner children's slots copied out: credits
       if (tid == 0 && up) {
-        if (nk > 0 && !lc[0]) red_max_relaxed(up_tail(c1), E | (uint64_t)(up_in + 1));
-        if (nk > 1 && !lc[1]) red_max_relaxed(up_tail(c2), E | (uint64_t)(up_in + 1));
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (i < Rp.nk && !Rp.lc[i]) red_max_relaxed(up_tail(Rp.kid[i]), E | (uint64_t)(up_in + 1));
       }
       const unsigned char* xs = xbuf + (size_t)st.b * xstage;
       const unsigned char* p1 = p1buf + (size_t)st.b * pstage;
@@ -385,12 +465,14 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
         }
         Acc s;
         acc_init<DT>(s, u < nx ? lds128(xs + (size_t)u * 16) : ld_partial<DT>(xg + gu * 16, v));
-        // the left child's partial, then the right child's: accumulator
-        // words from an inner child, the element type from a leaf's input
-        for (int i = 0; i < nk; ++i) {
+        // the first child's partial, then the second's: accumulator words
+        // from an inner child, the element type from a leaf's input
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (i >= Rp.nk) break;
           const unsigned char* pi = i == 0 ? p1 : p2;
-          if (lc[i]) {
-            const char* cg = static_cast<const char*>(a.in[i == 0 ? c1 : c2]);
+          if (Rp.lc[i]) {
+            const char* cg = static_cast<const char*>(a.in[Rp.kid[i]]);
             acc_add<DT>(s, u < nx ? lds128(pi + (size_t)u * 16) : ld_partial<DT>(cg + gu * 16, v));
           } else {
             uint4 w[2];
@@ -419,7 +501,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __gr
         st_release_cta_u32(&sh.done[cw], q + 1);
       }
       if (up) {
-        if (nk > 0) ++up_in;
+        ++up_in;
         if (send_up && ++up_slot == (uint32_t)K) up_slot = 0;
       }
     }

@@ -25,7 +25,6 @@ constexpr int kStaticMaxChannels = 16;
 constexpr size_t kStaticFlagWords = (size_t)kMaxRanks * kStaticMaxChannels * kMaxWarps;  // 2048
 constexpr size_t kStaticFlagOffset = 256;
 constexpr size_t kStaticScratchBytes = kStaticFlagOffset + kStaticFlagWords * sizeof(uint64_t);  // 16640
-constexpr uint64_t kStaticTimeoutNs = 500ull * 1000 * 1000;
 constexpr int kMaxDevices = 64;
 
 // [0, 64): DevStatus   [64, 128): SyncHdr   [256, ...): progress flags
@@ -58,6 +57,10 @@ cudaError_t scratch_for_current_device(char** out) {
   return cudaSuccess;
 }
 
+cudaStream_t stream_of(rra_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+constexpr const char* kCall = "allreduce_two_shot_static";
+
 bool ranges_overlap(const void* a, size_t an, const void* b, size_t bn) {
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
   return an && bn && x < y + bn && y < x + an;
@@ -71,25 +74,26 @@ using namespace rra;
 extern "C" rra_status_t rra_allreduce_two_shot_static(const void* const* bufs, void* const* outs,
                                                       int nranks, size_t count, rra_dtype_t dtype,
                                                       rra_op_t op, rra_stream_t stream) {
+  auto fail = [&](rra_status_t e) { return record_call(kCall, RRA_ALGO_TWO_SHOT, nranks, count, dtype, 0, e); };
   if (!bufs || !outs || nranks < 1 || op != RRA_SUM ||
       (dtype != RRA_INT32 && dtype != RRA_FLOAT32 && dtype != RRA_BFLOAT16))
-    return RRA_ERR_INVALID_ARG;
-  if (nranks > kMaxRanks) return RRA_ERR_UNSUPPORTED;  // the static flags hold 8 ranks at most
+    return fail(nranks > kMaxRanks ? RRA_ERR_UNSUPPORTED : RRA_ERR_INVALID_ARG);
+  if (nranks > kMaxRanks) return fail(RRA_ERR_UNSUPPORTED);  // the static flags hold 8 ranks at most
   const size_t e = dtype == RRA_BFLOAT16 ? 2 : 4;
-  if (count > (SIZE_MAX / 2) / e) return RRA_ERR_INVALID_ARG;
+  if (count > (SIZE_MAX / 2) / e) return fail(RRA_ERR_INVALID_ARG);
   const size_t S = count * e;
   for (int r = 0; r < nranks; ++r)
-    if (!bufs[r] || !outs[r] || (uintptr_t)bufs[r] % e || (uintptr_t)outs[r] % e) return RRA_ERR_INVALID_ARG;
+    if (!bufs[r] || !outs[r] || (uintptr_t)bufs[r] % e || (uintptr_t)outs[r] % e) return fail(RRA_ERR_INVALID_ARG);
   for (int i = 0; i < nranks; ++i)
     for (int j = 0; j < nranks; ++j) {
-      if (i < j && ranges_overlap(outs[i], S, outs[j], S)) return RRA_ERR_ALIAS;
-      if (ranges_overlap(outs[j], S, bufs[i], S) && !(i == j && outs[j] == bufs[i])) return RRA_ERR_ALIAS;
+      if (i < j && ranges_overlap(outs[i], S, outs[j], S)) return fail(RRA_ERR_ALIAS);
+      if (ranges_overlap(outs[j], S, bufs[i], S) && !(i == j && outs[j] == bufs[i])) return fail(RRA_ERR_ALIAS);
     }
-  if (count == 0) return RRA_SUCCESS;
+  if (count == 0) return fail(RRA_SUCCESS);
 
   char* scratch = nullptr;
-  if (scratch_for_current_device(&scratch) != cudaSuccess) return RRA_ERR_CUDA;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (scratch_for_current_device(&scratch) != cudaSuccess)
+    return record_call(kCall, RRA_ALGO_TWO_SHOT, nranks, count, dtype, 0, RRA_ERR_CUDA);
 
   TwoShotArgs a{};
   const size_t pu = 16 / e;
@@ -107,7 +111,8 @@ extern "C" rra_status_t rra_allreduce_two_shot_static(const void* const* bufs, v
   }
   a.tile_units = kDirectThreads * twoshot_units_per_thread(nranks);
   int occ = 0, dev = 0, sms = 0;
-  if (twoshot_occupancy(nranks, dtype, vec, &occ) != cudaSuccess || occ < 1) return RRA_ERR_CUDA;
+  if (twoshot_occupancy(nranks, dtype, vec, &occ) != cudaSuccess || occ < 1)
+    return record_call(kCall, RRA_ALGO_TWO_SHOT, nranks, count, dtype, 0, RRA_ERR_CUDA);
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const size_t units0 = (a.chunk_len[0] + pu - 1) / pu;
@@ -115,18 +120,38 @@ extern "C" rra_status_t rra_allreduce_two_shot_static(const void* const* bufs, v
   if (c < 1) c = 1;
   if (c > (size_t)kStaticMaxChannels) c = kStaticMaxChannels;
   if (c > (size_t)(sms * occ / nranks)) c = (size_t)(sms * occ / nranks);
-  if (c < 1) return RRA_ERR_UNSUPPORTED;
-  if ((size_t)nranks * c * kMaxWarps > kStaticFlagWords) return RRA_ERR_UNSUPPORTED;
+  if (c > (size_t)channels_allowed(nranks)) c = (size_t)channels_allowed(nranks);  // the SM budget
+  if (c < 1 || (size_t)nranks * c * kMaxWarps > kStaticFlagWords)
+    return record_call(kCall, RRA_ALGO_TWO_SHOT, nranks, count, dtype, 0, RRA_ERR_UNSUPPORTED);
   a.channels = (int)c;
   a.progress = reinterpret_cast<uint64_t*>(scratch + kStaticFlagOffset);
   a.wait.status = reinterpret_cast<DevStatus*>(scratch);
   a.wait.sync = reinterpret_cast<SyncHdr*>(scratch + 64);
-  a.wait.timeout_ns = kStaticTimeoutNs;
-  a.wait.skip_rank = -1;
-  // The status block must start each call at zero; the epoch and the
-  // arrival counter carry over (the last CTA of each call resets the
-  // counter and bumps the epoch, so the flags never need clearing).
-  if (cudaMemsetAsync(scratch, 0, sizeof(DevStatus), st) != cudaSuccess) return RRA_ERR_CUDA;
-  if (launch_twoshot(nranks, dtype, vec, a, nranks * (int)c, st) != cudaSuccess) return RRA_ERR_CUDA;
-  return RRA_SUCCESS;
+  a.wait.timeout_ns = current_timeout_ns();
+  a.wait.skip_rank = current_skip_rank();
+  // The status block keeps the first device error until
+  // rra_query_status_static reads and clears it (a stale abort tag never
+  // matches a later call's tag); the epoch and the arrival counter carry
+  // over (the last CTA of each call resets the counter and bumps the epoch,
+  // so the flags never need clearing).
+  const rra_status_t st = launch_twoshot(nranks, dtype, vec, a, nranks * (int)c, stream_of(stream)) == cudaSuccess
+                              ? RRA_SUCCESS
+                              : RRA_ERR_CUDA;
+  return record_call(kCall, RRA_ALGO_TWO_SHOT, nranks, count, dtype, nranks * (int)c, st);
+}
+
+extern "C" rra_status_t rra_query_status_static(rra_stream_t stream, int32_t info[4]) {
+  if (info) info[0] = info[1] = info[2] = info[3] = 0;
+  if (cudaStreamSynchronize(stream_of(stream)) != cudaSuccess) return RRA_ERR_CUDA;
+  char* scratch = nullptr;
+  if (scratch_for_current_device(&scratch) != cudaSuccess) return RRA_ERR_CUDA;
+  DevStatus h{};
+  if (cudaMemcpy(&h, scratch, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return RRA_ERR_CUDA;
+  if (h.code == 0) return RRA_SUCCESS;
+  if (info) decode_status(h, info);
+  // clear the record; the abort tag belongs to a finished call and can stay
+  DevStatus z{};
+  z.abort_tag = h.abort_tag;
+  if (cudaMemcpy(scratch, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return RRA_ERR_CUDA;
+  return (rra_status_t)h.code;
 }

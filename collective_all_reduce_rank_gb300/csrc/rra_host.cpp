@@ -350,7 +350,7 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
   a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", 2L * a.G));
   if ((size_t)c * n * a.K * a.slot_bytes > s->ws.fifo_bytes) a.K = a.G + 1;
   c = std::min<long>(c, (long)(s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes)));
-  if (c < 1) return RRA_ERR_UNSUPPORTED;
+  if (c < 1) return RRA_ERR_WORKSPACE;
   // messages per CTA stay below 2^31 (32-bit counters in the kernel)
   const size_t trips = (maxu + (size_t)c * a.G * T - 1) / ((size_t)c * a.G * T);
   if (trips * (size_t)(2 * n) * a.G >= (1ull << 31)) return RRA_ERR_UNSUPPORTED;
@@ -362,20 +362,18 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
   return cuda_status(launch_ring_staged(dt, a, n * (int)c, st));
 }
 
-// Staged tree: one message per tile of T units (T <= RRA_TREE_TILE: 2048 for
-// 4-byte types, 1024 for bfloat16, whose partials travel as float32), G
-// tiles per iteration (RRA_TREE_G, 24), K = G + 1 FIFO slots per up link
-// (RRA_TREE_K), the broadcast L iterations behind the reduction
-// (RRA_TREE_LAG: 6, 4 for bfloat16), stages as shared memory allows; T
-// balanced over whole iterations as in the staged ring.  Measured on GB300
-// at 8 x 100 MB fp32: larger tiles pay for fewer stages (T 1024: 1.77 TB/s,
-// 2048: 2.25); G hides the up-and-back wave of each iteration until the
-// FIFO crowds L2 (G 12: 1.95, 24: 2.25, 32: 2.04 at T 2048); a lag of 6
-// gives 2.48.
+// Staged double binary tree: the message split in two by the chunk plan for
+// two parts (the first part on tree 0, the rest on tree 1); one message per
+// tile of T units (T <= RRA_TREE_TILE: 2048 for 4-byte types, 1024 for
+// bfloat16, whose partials travel as float32), G tiles per iteration
+// (RRA_TREE_G), K = G + 1 FIFO slots per up link (RRA_TREE_K), the
+// broadcast L iterations behind the reduction (RRA_TREE_LAG), stages as
+// shared memory allows; T balanced over whole iterations of one part as in
+// the staged ring.
 rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* out, int n, size_t count,
                              rra_dtype_t dt, cudaStream_t st, int* grid_out) {
   StagedTreeArgs a{};
-  const size_t e = elem_size(dt), aw = dt == RRA_BFLOAT16 ? 2 : 1;
+  const size_t e = elem_size(dt), aw = dt == RRA_BFLOAT16 ? 2 : 1, pu = 16 / e;
   for (int r = 0; r < n; ++r) {
     a.in[r] = in[r];
     a.out[r] = out[r];
@@ -383,6 +381,10 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   a.n = n;
   a.count = count;
   const size_t units = (count * e + 15) / 16;
+  // chunk plan for two parts: H = ceil(count / 2) rounded up to whole units
+  const size_t h = std::min(count, ((count + 1) / 2 + pu - 1) / pu * pu);
+  a.half_units = (h + pu - 1) / pu;
+  const size_t part = std::max(a.half_units, units - a.half_units);  // units of the larger part
   a.G = (int)std::max(1L, env_long("RRA_TREE_G", 24));
   a.lag = (int)std::max(1L, std::min(64L, env_long("RRA_TREE_LAG", aw == 2 ? 4 : 6)));
   const long tmax = std::max(64L, std::min(4096L, env_long("RRA_TREE_TILE", aw == 2 ? 1024 : 2048)));
@@ -396,11 +398,11 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   const long cmax = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), channel_cap(n)});
   if (cmax < 1) return RRA_ERR_UNSUPPORTED;
   const size_t G = (size_t)a.G;
-  long c = std::min<long>({cmax, (long)std::max<size_t>(1, (units + G * 128 - 1) / (G * 128)),
+  long c = std::min<long>({cmax, (long)std::max<size_t>(1, (part + G * 128 - 1) / (G * 128)),
                            env_long("RRA_TREE_CHANNELS", cmax)});
   c = std::max(1L, c);
-  const size_t iters = std::max<size_t>(1, (units + (size_t)c * G * tmax - 1) / ((size_t)c * G * tmax));
-  long T = (long)((units + (size_t)c * G * iters - 1) / ((size_t)c * G * iters));
+  const size_t iters = std::max<size_t>(1, (part + (size_t)c * G * tmax - 1) / ((size_t)c * G * tmax));
+  long T = (long)((part + (size_t)c * G * iters - 1) / ((size_t)c * G * iters));
   T = std::max(32L, std::min(tmax, (T + 31) / 32 * 32));
   a.slice_units = (int)T;
   a.stages = stages_for(T);
@@ -408,12 +410,14 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   a.slot_bytes = (size_t)T * 16 * aw;
   a.K = (int)std::max((long)a.G + 1, env_long("RRA_TREE_K", (long)a.G + 1));
-  // one up FIFO per node and channel (the totals come down from outputs)
+  // one up FIFO per rank and channel (a rank sends up in one tree at most;
+  // the totals come down from outputs)
   if ((size_t)c * n * a.K * a.slot_bytes > s->ws.fifo_bytes) a.K = a.G + 1;
   c = std::min<long>(c, (long)(s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes)));
-  if (c < 1 || (size_t)2 * n * c > kLinkFlags) return RRA_ERR_UNSUPPORTED;
-  const size_t trips = (units + (size_t)c * a.G * T - 1) / ((size_t)c * a.G * T);
-  if (trips * 2 * (size_t)a.G >= (1ull << 31)) return RRA_ERR_UNSUPPORTED;
+  if (c < 1 || (size_t)2 * n * c > kLinkFlags) return RRA_ERR_WORKSPACE;
+  // messages per CTA (both trees) stay below 2^31
+  const size_t trips = (part + (size_t)c * a.G * T - 1) / ((size_t)c * a.G * T);
+  if (trips * 4 * (size_t)a.G >= (1ull << 31)) return RRA_ERR_UNSUPPORTED;
   a.channels = (int)c;
   a.fifo = s->ws.fifo;
   a.head = s->ws.flags;
@@ -512,6 +516,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   const size_t fifo_cap = s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes);
   long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
                            (long)fifo_cap, env_long("RRA_RING_CHANNELS", 16), channel_cap(n)});
+  if (fifo_cap < 1) return RRA_ERR_WORKSPACE;
   if (c < 1) return RRA_ERR_UNSUPPORTED;
   if (proto == kProtoLL) {
     // LL line flags carry the slot round in 12 bits: more rounds than that
@@ -526,6 +531,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
       const size_t cap2 = s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes);
       c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
                           (long)cap2, env_long("RRA_RING_CHANNELS", 16), channel_cap(n)});
+      if (cap2 < 1) return RRA_ERR_WORKSPACE;
       if (c < 1) return RRA_ERR_UNSUPPORTED;
       a.channels = (int)c;
       a.fifo = s->ws.fifo;
@@ -574,6 +580,27 @@ void load_default_tuning() {
 
 }  // namespace
 
+uint64_t rra::current_timeout_ns() { return timeout_ns(); }
+
+int rra::current_skip_rank() { return g_skip_rank.load(); }
+
+long rra::channels_allowed(int n) { return channel_cap(n); }
+
+rra_status_t rra::record_call(const char* call, int algo, int n, size_t count, int dt, int grid, rra_status_t st) {
+  return record(call, algo, n, count, dt, grid, st);
+}
+
+// Prefer the wait on a peer that never posted: it names the rank that did
+// not join, not one stuck behind it.
+void rra::decode_status(const DevStatus& h, int32_t info[4]) {
+  const unsigned long long d = h.root_detail ? h.root_detail : h.detail;
+  const int peer = (int)((d >> 16) & 0xFFFF);
+  info[0] = h.code;
+  info[1] = (int)(d & 0xFFFF);
+  info[2] = peer == 0xFFFF ? -1 : peer;
+  info[3] = (int)((d >> 32) & 0x7FFFFFFF);
+}
+
 int rra::max_ctas_cap() {
   int m = g_max_ctas.load();
   if (m < 0) {
@@ -597,6 +624,7 @@ const char* rra_status_string(rra_status_t s) {
     case RRA_ERR_NOT_INITIALIZED: return "rra_init was not called for this device";
     case RRA_ERR_CUDA: return "CUDA error";
     case RRA_ERR_TIMEOUT: return "device wait timed out";
+    case RRA_ERR_WORKSPACE: return "workspace too small for the call (rra_init workspace_bytes)";
     default: return "unknown status";
   }
 }
@@ -632,18 +660,19 @@ rra_status_t rra_init(int device, size_t workspace_bytes) {
   return RRA_SUCCESS;
 }
 
-rra_status_t rra_finalize(int device) {
-  if (device < 0 || device >= kMaxDevices) return RRA_ERR_INVALID_ARG;
+rra_status_t rra_finalize(void) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
-  DevState& s = g_dev[device];
-  if (!s.ready) return RRA_SUCCESS;
   int cur = 0;
-  cudaGetDevice(&cur);
-  cudaSetDevice(device);
-  cudaFree(s.base);
-  cudaSetDevice(cur);
-  s = DevState{};
-  return RRA_SUCCESS;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  rra_status_t st = RRA_SUCCESS;
+  for (int d = 0; d < kMaxDevices; ++d) {
+    DevState& s = g_dev[d];
+    if (!s.ready) continue;
+    if (cudaSetDevice(d) != cudaSuccess || cudaFree(s.base) != cudaSuccess) st = RRA_ERR_CUDA;
+    s = DevState{};
+  }
+  if (have_cur) cudaSetDevice(cur);
+  return st;
 }
 
 void rra_set_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns); }
@@ -760,7 +789,11 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
       a.out[r] = outs[r];
     }
     a.count = count;
-    a.per_rank_grid = (int)env_long("RRA_ONESHOT_PER_RANK", 0) != 0;
+    // the literal per-rank form reads every input while other ranks write
+    // their outputs, so in place it would need the barrier one-shot has
+    // between its reads and writes on n GPUs; in place takes the combined
+    // form, which reads a unit of all n inputs before it writes any output
+    a.per_rank_grid = (int)env_long("RRA_ONESHOT_PER_RANK", 0) != 0 && !inplace_all;
     if (vec && !a.per_rank_grid && env_long("RRA_ONESHOT_TMA", 0) != 0 && count * e >= 16) {
       // whole 16-byte units by bulk copies, the sub-unit tail by the LSU kernel
       const size_t units = count * e / 16;
@@ -790,20 +823,8 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
   if (!s || !s->ready) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_NOT_INITIALIZED);
   int grid = 0;
   rra_status_t rs;
-  // the cluster form only without fault injection: a silent rank would
-  // leave its cluster peers at a hardware barrier
-  if (algo == RRA_ALGO_TREE && (env_long("RRA_TREE_CLUSTER", 0) == 0 || g_skip_rank.load() >= 0)) {
+  if (algo == RRA_ALGO_TREE) {
     rs = run_tree_staged(s, bufs, outs, nranks, count, dtype, st, &grid);
-  } else if (algo == RRA_ALGO_TREE) {
-    const int maxc = tree_max_clusters(nranks, dtype);
-    if (maxc <= 0) return record(call, algo, nranks, count, dtype, 0, RRA_ERR_UNSUPPORTED);
-    const int G = (int)std::max(1L, std::min(4L, env_long("RRA_TREE_G", 2)));
-    const size_t tu = (size_t)tree_tile_units_for(dtype);
-    const size_t tiles = (count * e / 16 + tu - 1) / tu;
-    long c = std::min<long>({(long)maxc, (long)std::max<size_t>(1, (tiles + G - 1) / G), channel_cap(nranks)});
-    c = std::min(c, env_long("RRA_TREE_CHANNELS", c));
-    grid = nranks * (int)std::max(1L, c);
-    rs = cuda_status(launch_tree(dtype, bufs, outs, nranks, count, (int)std::max(1L, c), G, wait_cfg(s), st));
   } else if (algo == RRA_ALGO_TWO_SHOT) {
     rs = run_twoshot(s, bufs, outs, nranks, count, dtype, vec, st, &grid);
   } else {
@@ -1086,16 +1107,7 @@ rra_status_t rra_query_status(rra_stream_t stream, int32_t info[4]) {
   DevStatus h{};
   if (cudaMemcpy(&h, s->ws.status, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return RRA_ERR_CUDA;
   if (h.code == 0) return RRA_SUCCESS;
-  if (info) {
-    // prefer the wait on a peer that never posted: it names the rank that
-    // did not join, not one stuck behind it
-    const unsigned long long d = h.root_detail ? h.root_detail : h.detail;
-    const int peer = (int)((d >> 16) & 0xFFFF);
-    info[0] = h.code;
-    info[1] = (int)(d & 0xFFFF);
-    info[2] = peer == 0xFFFF ? -1 : peer;
-    info[3] = (int)((d >> 32) & 0x7FFFFFFF);
-  }
+  if (info) decode_status(h, info);
   // clear the record; the abort tag belongs to a finished call and can stay
   DevStatus z{};
   z.abort_tag = h.abort_tag;

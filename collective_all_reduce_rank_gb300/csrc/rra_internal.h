@@ -115,13 +115,15 @@ struct RingArgs {
   WaitCfg wait;
 };
 
-// Staged tree all-reduce (persistent, cooperative).  Per channel: up FIFO
-// of inner node r at link r; heads [2n x channels] (up, then down); tails
+// Staged double binary tree all-reduce (persistent, cooperative).  A rank
+// sends up and posts down in at most one of the two trees, so per channel:
+// up FIFO of rank r at link r; heads [2n x channels] (up, then down); tails
 // [n x channels] (up); joined flags [n x channels].
 struct StagedTreeArgs {
   const void* in[kMaxRanks];
   void* out[kMaxRanks];
-  size_t count;  // elements per rank
+  size_t count;       // elements per rank
+  size_t half_units;  // 16-byte units of the part reduced on tree 0 (the rest: tree 1)
   char* fifo;    // n up links x channels x K slots x slot_bytes
   uint64_t* head;
   uint64_t* tail;
@@ -167,6 +169,18 @@ constexpr int kLLThreads = 256;
 // grids with it.
 int max_ctas_cap();
 
+// Settings of rra_host.cpp that the allocation-free entry point
+// (noalloc.cu) honours too: the bound of device waits
+// (rra_set_timeout_ns), the rank fault injection silences
+// (rra_debug_skip_rank), the channels per rank the SM budget leaves, the
+// flight recorder, and the decoding of a status block into {code, rank,
+// peer, index}.
+uint64_t current_timeout_ns();
+int current_skip_rank();
+long channels_allowed(int n);
+rra_status_t record_call(const char* call, int algo, int n, size_t count, int dt, int grid, rra_status_t st);
+void decode_status(const DevStatus& h, int32_t info[4]);
+
 // Streaming kernels: `units` 16-byte units per grid row; *grid receives the
 // CTAs per row launched.
 cudaError_t launch_oneshot(int n, int dt, bool vec, const DirectArgs& a, size_t units, int* grid,
@@ -203,13 +217,6 @@ int ring_cluster_tile_units(int dt);
 int ring_cluster_slots(int dt);
 int ring_cluster_max_clusters(int n, int dt);
 cudaError_t launch_ring_cluster(int dt, const RingArgs& a, int grid, cudaStream_t s);
-
-// Tree all-reduce on thread-block clusters of n CTAs (16-byte aligned
-// buffers): `channels` clusters, G tiles per batch (G <= 4).
-int tree_tile_units_for(int dt);
-int tree_max_clusters(int n, int dt);
-cudaError_t launch_tree(int dt, const void* const* in, void* const* out, int n, size_t count, int channels, int G,
-                        const WaitCfg& w, cudaStream_t s);
 
 // Ring with whole-CTA messages staged in shared memory (Simple protocol):
 // 16-byte aligned buffers and chunk starts; one link counter per (link,

@@ -71,12 +71,12 @@
  *                        bfloat16), tiles per iteration (24), FIFO slots
  *                        (G + 1), iterations the broadcast trails the
  *                        reduction (6, 4 for bfloat16), stages, CTAs per rank
- *   RRA_TREE_CLUSTER     1: the tree on thread-block clusters
  *   RRA_TWOSHOT_CLUSTER  1: two-shot on thread-block clusters
  *   RRA_TWOSHOT_CHANNELS CTAs per rank of two-shot
  *   RRA_ONESHOT_TMA      1: one-shot with bulk copies through shared memory
  *   RRA_ONESHOT_PER_RANK 1: one-shot reads the n inputs once per rank, as
- *                        n GPUs would
+ *                        n GPUs would (out of place only; in place keeps
+ *                        the combined form)
  */
 #ifndef RRA_H
 #define RRA_H
@@ -95,13 +95,16 @@ typedef struct CUstream_st* rra_stream_t;
 #define RRA_MAX_RANKS 8
 
 typedef enum {
-  RRA_SUCCESS = 0,
+  RRA_OK = 0,
+  RRA_SUCCESS = RRA_OK,        /* the same value under a second name */
   RRA_ERR_INVALID_ARG = 1,     /* null pointer, bad count, bad enum, misaligned pointer, flag 0 */
   RRA_ERR_UNSUPPORTED = 2,     /* valid but not supported here (e.g. nranks > RRA_MAX_RANKS) */
   RRA_ERR_ALIAS = 3,           /* input and output ranges overlap other than in place */
   RRA_ERR_NOT_INITIALIZED = 4, /* rra_init() was not called for the current device */
   RRA_ERR_CUDA = 5,            /* a CUDA runtime call failed (launch, query) */
-  RRA_ERR_TIMEOUT = 6          /* a bounded device wait expired (see rra_query_status) */
+  RRA_ERR_TIMEOUT = 6,         /* a bounded device wait expired (see rra_query_status) */
+  RRA_ERR_WORKSPACE = 7        /* the workspace of rra_init is too small for the call's FIFO
+                                  slots and flags (call rra_init with more workspace_bytes) */
 } rra_status_t;
 
 typedef enum { RRA_INT32 = 0, RRA_FLOAT32 = 1, RRA_BFLOAT16 = 2 } rra_dtype_t;
@@ -121,12 +124,18 @@ typedef enum {
    *  (cudaMemcpyAsync device to device), no SM runs a kernel ([AIH]
    *  "Protocols": transfer methods that use no SMs, like the copy engine). */
   RRA_ALGO_COPY_ENGINE = 5,
-  /** all-reduce only: reduce up a binary tree, broadcast down it ([AIH]
-   *  "Algorithms": tree, O(log n) steps).  Heap order (parent of r is
-   *  (r-1)/2); node r sums its own data, then its left child's partial,
-   *  then its right child's; the root's total, rounded once, travels down
-   *  unchanged.  Needs 16-byte aligned buffers.  Links through the
-   *  workspace (RRA_TREE_CLUSTER=1: through thread-block clusters). */
+  /** all-reduce only: a double binary tree ([AIH] "Algorithms": tree
+   *  (double binary tree), reduce up, broadcast down, O(log n) steps,
+   *  large messages pipelined in chunks).  Tree 0 is the binary tree in
+   *  heap order over the ranks (position p has children 2p+1 and 2p+2,
+   *  rank r at position r), tree 1 the same tree over the ranks reversed
+   *  (rank r at position n-1-r).  The first part of the message by the
+   *  chunk plan for two parts (C = ceil(count/2) rounded up to whole
+   *  16-byte vectors) is reduced on tree 0, the rest on tree 1.  A node
+   *  sums its own data, then the partial of its child 2p+1, then that of
+   *  its child 2p+2; each root's total, rounded once, travels down
+   *  unchanged.  Needs 16-byte aligned buffers (else
+   *  RRA_ERR_UNSUPPORTED).  Links through the workspace. */
   RRA_ALGO_TREE = 6
 } rra_algo_t;
 
@@ -144,9 +153,13 @@ typedef enum {
  *  RRA_ERR_CUDA (allocation failed). */
 rra_status_t rra_init(int device, size_t workspace_bytes);
 
-/** Free the state of `device`.  The caller must have synchronized every
- *  stream that used it. */
-rra_status_t rra_finalize(int device);
+/** Free the state rra_init made on every device (the pages' communicator
+ *  teardown that ends the "init step before calls" of [ILP] "Code").  The
+ *  caller must have synchronized every stream that used it; later calls
+ *  that need the workspace return RRA_ERR_NOT_INITIALIZED until rra_init
+ *  is called again.  Returns RRA_ERR_CUDA if freeing a workspace failed
+ *  (the state is dropped all the same). */
+rra_status_t rra_finalize(void);
 
 /* ------------------------------------------------------------------------ */
 /* collectives                                                              */
@@ -179,7 +192,7 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
  *  memory, and so cannot call rra_init (which calls cudaMalloc for its
  *  workspace).  Examples: a plugin inside a framework whose allocator owns
  *  all device memory, or code under a memory budget that forbids new
- *  allocations after start-up.
+ *  allocations after start-up.  It needs no rra_init.
  *  - Same arguments, result and summation order as rra_allreduce with
  *    RRA_ALGO_TWO_SHOT (outs[r][i] = SUM_k bufs[k][i], chunk r reduced in
  *    ascending rank order, then gathered back).  The caller passes the
@@ -189,23 +202,35 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
  *    GPU that loads the library holds until the process exits.  It holds
  *    flags for at most 8 ranks x 16 channels; more than 8 ranks is
  *    RRA_ERR_UNSUPPORTED.  Messages of any size are split over at most 16
- *    channels per rank.
+ *    channels per rank (fewer under rra_set_max_ctas).
  *  - No cudaMalloc, cudaFree or allocating library routine is called.
  *    The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first
  *    call before any stream capture.
  *  - Every call on a device shares the one array, which keeps the last
- *    call's contents (the status block is cleared at the start of each
- *    call; the flags carry a per-call epoch and need no clearing).  Calls
- *    that overlap on the GPU -- on two streams without ordering, or
- *    together with another copy of this call -- race on it.
- *  - Device waits are bounded (500 ms); a wait that expires ends the
- *    kernel early, and this entry point offers no status query for it.
+ *    call's contents (the flags carry a per-call epoch and need no
+ *    clearing; the status block keeps the first device error until
+ *    rra_query_status_static reads and clears it).  Calls that overlap on
+ *    the GPU -- on two streams without ordering, or together with another
+ *    copy of this call -- race on it.
+ *  - Device waits are bounded by rra_set_timeout_ns; a wait that expires
+ *    ends the kernel early with the outputs partly written, and
+ *    rra_query_status_static then returns RRA_ERR_TIMEOUT.  Honours
+ *    rra_debug_skip_rank.  Recorded in rra_dump_recent.
  *  Errors: RRA_ERR_INVALID_ARG, RRA_ERR_UNSUPPORTED, RRA_ERR_ALIAS,
  *  RRA_ERR_CUDA.  count == 0 returns RRA_SUCCESS without a launch. */
 rra_status_t rra_allreduce_two_shot_static(const void* const* bufs, void* const* outs, int nranks,
                                            size_t count, rra_dtype_t dtype, rra_op_t op,
                                            rra_stream_t stream);
+
+/** Status of rra_allreduce_two_shot_static on the current device, which
+ *  allocates nothing either (the pages have no counterpart; it reads the
+ *  static scratch array of that entry point, not the workspace of
+ *  rra_init).  Synchronizes `stream`, copies the status block to the host
+ *  and clears it.  Returns RRA_SUCCESS, the first device error recorded
+ *  since the last query (RRA_ERR_TIMEOUT), or RRA_ERR_CUDA.  info (may be
+ *  NULL) receives {code, rank, peer, index} as rra_query_status gives it. */
+rra_status_t rra_query_status_static(rra_stream_t stream, int32_t info[4]);
 
 /** Reduce-scatter ([ILP] "Direct answer": sum across ranks, each keeps only
  *  its slice).  bufs[r] holds nranks*recvcount elements; outs[r]
@@ -304,12 +329,15 @@ rra_status_t rra_ll128_unpack(const void* const* wires, int nsrc, void* out, siz
 /* status, selection, configuration                                         */
 /* ------------------------------------------------------------------------ */
 
-/** Synchronize `stream`, then read and clear the current device's status
- *  word.  Returns RRA_SUCCESS, the recorded device error (RRA_ERR_TIMEOUT)
- *  or RRA_ERR_CUDA if the stream itself failed.  info (may be NULL)
- *  receives {code, rank, peer, index}: the rank (or LL source) whose wait
- *  expired, the rank it waited for (-1 if none) and the step (ring,
- *  two-shot) or line (LL, LL128) index. */
+/** The asynchronous error of the calls issued so far, as NCCL reports an
+ *  asynchronous communicator error ([AIH] "Common environment variables
+ *  and debugging": a collective that hangs or fails is found from the
+ *  device side, not from the launch).  Synchronize `stream`, then read and
+ *  clear the current device's status word.  Returns RRA_SUCCESS, the
+ *  recorded device error (RRA_ERR_TIMEOUT) or RRA_ERR_CUDA if the stream
+ *  itself failed.  info (may be NULL) receives {code, rank, peer, index}:
+ *  the rank (or LL source) whose wait expired, the rank it waited for (-1
+ *  if none) and the step (ring, two-shot) or line (LL, LL128) index. */
 rra_status_t rra_query_status(rra_stream_t stream, int32_t info[4]);
 
 /** The schedule AUTO uses for an all-reduce of bytes_per_rank bytes per
@@ -322,16 +350,22 @@ rra_status_t rra_query_status(rra_stream_t stream, int32_t info[4]);
  *  one-shot at every size.  Never returns RRA_ALGO_AUTO. */
 rra_algo_t rra_select_algo(int nranks, size_t bytes_per_rank, rra_dtype_t dtype);
 
-/** Load a tuning table: text lines "nranks dtype log2_bytes algo" (dtype
- *  int32|float32|bfloat16, algo ring|one_shot|two_shot); '#' starts a
- *  comment.  The entry with the largest log2_bytes <= ceil(log2(bytes))
+/** Load a tuning table ([AIH] "Algorithms": the alpha-beta crossovers are
+ *  only illustrative and must be measured on one's own machine; this is
+ *  where the measured ones go): text lines "nranks dtype log2_bytes algo"
+ *  (dtype int32|float32|bfloat16, algo ring|one_shot|two_shot|tree); '#'
+ *  starts a comment.  The entry with the largest log2_bytes <= ceil(log2(bytes))
  *  for (nranks, dtype) wins.  NULL clears the table.  Errors:
  *  RRA_ERR_INVALID_ARG (unreadable or malformed file; the old table stays). */
 rra_status_t rra_load_tuning(const char* path);
 
 /** Upper bound, in nanoseconds of %globaltimer, on every device-side wait
- *  (ring and two-shot step flags, LL/LL128 line flags).  Default 500 ms
- *  or RRA_TIMEOUT_NS from the environment; 0 restores the default. */
+ *  (ring, tree and two-shot step flags, LL/LL128 line flags).  [AIH]
+ *  "Common environment variables and debugging" describes collectives that
+ *  wait forever for a rank that never arrives; here every such wait ends
+ *  after this bound with RRA_ERR_TIMEOUT in the status word.  Default 500
+ *  ms or RRA_TIMEOUT_NS from the environment; 0 restores the default.
+ *  Also bounds the waits of rra_allreduce_two_shot_static. */
 void rra_set_timeout_ns(uint64_t ns);
 
 /** SM budget ([AIH] "Protocols": each channel is a CUDA block, and
@@ -343,12 +377,14 @@ void rra_set_timeout_ns(uint64_t ns);
 void rra_set_max_ctas(int max_ctas);
 
 /** Fault injection for tests: virtual rank `rank` posts no step flag in the
- *  following ring, two-shot and tree calls (-1 turns it off), so its peers'
- *  waits expire with RRA_ERR_TIMEOUT naming it as `peer`.  The GPU stays
- *  usable. */
+ *  following ring, two-shot (also rra_allreduce_two_shot_static) and tree
+ *  calls (-1 turns it off), so its peers' waits expire with RRA_ERR_TIMEOUT
+ *  naming it as `peer`.  The GPU stays usable. */
 void rra_debug_skip_rank(int rank);
 
-/** Static text for a status code. */
+/** Static text for a status code, for the error reports [AIH] "Common
+ *  environment variables and debugging" asks to read first when a
+ *  collective fails. */
 const char* rra_status_string(rra_status_t status);
 
 /** Flight recorder ([AIH] "Common environment variables and debugging":

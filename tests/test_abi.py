@@ -25,9 +25,15 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
-        assert rra.rra_status_string(code)
+    for code in range(8):
+        assert rra.rra_status_string(code) != "unknown status", code
     assert "timed out" in rra.rra_status_string(rra.RRA_ERR_TIMEOUT)
+    assert "workspace" in rra.rra_status_string(rra.RRA_ERR_WORKSPACE)
+    assert rra.RRA_OK == rra.RRA_SUCCESS == 0
+
+
+def test_finalize_without_init_is_a_no_op(lib):
+    assert rra.rra_finalize() == rra.RRA_OK
 
 
 @pytest.mark.parametrize("B", [0, 1, 3, 4, 5, 119, 120, 121, 1 << 20])

@@ -56,6 +56,37 @@ def test_crashed_rank_times_out_and_gpu_stays_usable(algo, proto, skip, monkeypa
         g.assert_bits_equal(g.to_host(outs[r], "float32"), want[r], "after recovery")
 
 
+@pytest.mark.parametrize("skip", [0, 3])
+def test_static_two_shot_silent_rank_times_out_and_recovers(skip):
+    # the allocation-free two-shot honours the wait bound and the fault
+    # injection, and reports through its own status query
+    import gpu_util as g
+
+    n, count = 4, 1 << 20
+    xs = inputs.make_ranks(n, count, "float32", "normal", seed=2)
+    ins = [g.to_dev(x, "float32") for x in xs]
+    outs = g.empty(n, count, "float32")
+    rra.rra_set_timeout_ns(1_000_000)  # 1 ms
+    rra.rra_debug_skip_rank(skip)
+    try:
+        rra.rra_allreduce_two_shot_static(ins, outs, count, rra.RRA_FLOAT32)
+        st, info = rra.rra_query_status_static()
+    finally:
+        rra.rra_debug_skip_rank(-1)
+        rra.rra_set_timeout_ns(2_000_000_000)
+    assert st == rra.RRA_ERR_TIMEOUT and info[0] == rra.RRA_ERR_TIMEOUT
+    assert info[2] == skip, info
+    # the status was read and cleared; the next call is correct
+    rra.rra_allreduce_two_shot_static(ins, outs, count, rra.RRA_FLOAT32)
+    st, info = rra.rra_query_status_static()
+    assert st == 0, info
+    want, _, _ = oracle.allreduce("twoshot", xs, "float32")
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], "float32"), want[r], "static after recovery")
+    # the regular status word saw none of it
+    assert rra.rra_query_status()[0] == 0
+
+
 def test_flight_recorder_lists_recent_calls():
     import gpu_util as g
 

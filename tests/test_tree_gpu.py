@@ -89,37 +89,23 @@ def test_staged_tree_lag(lag, tile, G, K, stages, dtype, n, count, monkeypatch):
         g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "staged tree lag=%d n=%d r=%d" % (lag, n, r))
 
 
-@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
-@pytest.mark.parametrize("n,count", [(3, 100_003), (8, 3_000_001)])
-def test_cluster_tree_form(dtype, n, count, monkeypatch):
-    # the tree on thread-block clusters (links in distributed shared memory)
-    import gpu_util as g
-
-    monkeypatch.setenv("RRA_TREE_CLUSTER", "1")
-    xs = inputs.make_ranks(n, count, dtype, "normal", seed=count)
-    want, _, _ = oracle.allreduce("tree", xs, dtype)
-    ins = [g.to_dev(x, dtype) for x in xs]
-    outs = g.empty(n, count, dtype)
-    rra.rra_allreduce(ins, outs, count, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_TREE)
-    assert rra.rra_query_status()[0] == 0
-    for r in range(n):
-        g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "cluster tree n=%d r=%d" % (n, r))
-
-
 def test_tree_order_case_on_gpu():
-    # the hand-derived n = 4 case of the oracle's pins: (0, 1.5) per column
+    # the hand-derived n = 4 double-tree case of the oracle's pins, x =
+    # (0.5, 2^25, 2, -2^25) on every element of each rank: 2.5 on the part
+    # tree 0 sums, (x0 + (x1 + x3)) + x2, and 2 on tree 1's part,
+    # (x3 + (x2 + x0)) + x1; many tiles in each part
     import gpu_util as g
 
     B = float(2 ** 25)
-    cols = np.array([[0.5, 0.5], [B, B], [-B, 1.0], [0.0, -B]], np.float32)
-    xs = [np.tile(c, 2048) for c in cols]  # several tiles
+    count = 4 * 40_000
+    xs = [np.full(count, v, np.float32) for v in (0.5, B, 2.0, -B)]
     ins = [g.to_dev(x, "float32") for x in xs]
-    outs = g.empty(4, xs[0].size, "float32")
-    rra.rra_allreduce(ins, outs, xs[0].size, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE)
+    outs = g.empty(4, count, "float32")
+    rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE)
     assert rra.rra_query_status()[0] == 0
     for r in range(4):
-        got = g.to_host(outs[r], "float32").reshape(-1, 2)
-        assert np.all(got[:, 0] == 0.0) and np.all(got[:, 1] == 1.5)
+        got = g.to_host(outs[r], "float32")
+        assert np.all(got[: count // 2] == 2.5) and np.all(got[count // 2:] == 2.0), r
 
 
 def test_tree_rejects_unaligned():

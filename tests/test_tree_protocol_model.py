@@ -1,29 +1,33 @@
-"""A discrete-event model of the staged tree's link protocol
+"""A discrete-event model of the staged double binary tree's link protocol
 (kernels_tree_staged.cu), run on the CPU under random interleavings.
 
-Nodes are virtual ranks in heap order (parent of r is (r-1)/2).  A leaf's
-partial is its own input: it sends nothing up, and its parent reads the
-tile from the leaf's input.  Each inner non-root node r owns an up FIFO
-(its partial sums, read by its parent) of K
-slots with a head counter (messages posted by the writer's signaller) and a
-tail counter (messages the parent has copied out); the writer may reuse a
-slot once the tail has passed it.  The totals come down without a FIFO: a
-node with children stores each total in its own output and posts it on its
-down head counter, and both children read it from there (an output is
-written once, so it needs no credit).  A node's message
-sequence is, per iteration of G tiles: its G up messages, then (not at the
-root) the G down messages of the previous iteration, so the down wave of
-one iteration overlaps the up wave of the next.  Per CTA the roles are as
-in the staged ring: an X loader, P loaders taking messages round-robin (at
-most as many as stages), in-order consumers, a signaller; stages are
-tested by mbarrier phase parity.
+Two trees: tree 0 holds rank r at heap position r, tree 1 at position
+n-1-r (position p has children 2p+1, 2p+2 and parent (p-1)/2).  Each CTA
+(one rank here; channels are independent copies) serves both trees.  A leaf's
+partial is its own input: it sends nothing up, and its parent reads the tile
+from the leaf's input.  Each inner non-root node owns an up FIFO (its partial
+sums, read by its parent) of K slots with a head counter (messages posted by
+the writer's signaller) and a tail counter (messages the parent has copied
+out); the writer may reuse a slot once the tail has passed it.  The totals
+come down without a FIFO: a node with children stores each total in its own
+output and posts it on its down head counter, and both children read it from
+there (an output is written once, so it needs no credit).  A rank has
+children in one tree at most, so these links are one per rank.
+
+A rank's message sequence: at time t, its up messages of tile iteration t
+(in the tree where it has children), then the down messages of tile
+iteration t - lag of tree 0, then those of tree 1; G messages each.  Per CTA
+the roles are as in the staged ring: an X loader, P loaders taking messages
+round-robin (at most as many as stages), in-order consumers, a signaller;
+stages are tested by mbarrier phase parity.
 
 Checked: every run finishes (no deadlock), no slot is read before it is
 written or after it is reused, no output is read before it is posted, no
-parity test passes for a phase that has not completed, and every rank ends
-with the total summed in the order of
-"Collective communication: NCCL's algorithms and protocols ...", section
-"Algorithms" (tree), as the oracle reads it: p_r = (x_r + p_{2r+1}) + p_{2r+2}.
+parity test passes for a phase that has not completed, no rank posts up or
+down messages in both trees, and every rank ends with each part's total
+summed in the order of "Collective communication: NCCL's algorithms and
+protocols ...", section "Algorithms" (the double binary tree), as the oracle
+reads it: at each node p = (x + p_{2p+1}) + p_{2p+2}.
 """
 import random
 
@@ -34,85 +38,108 @@ class Aliasing(Exception):
     pass
 
 
-def is_leaf(n, r):
-    return r > 0 and 2 * r + 1 >= n
+def rank_at(t, n, pos):
+    return pos if t == 0 else n - 1 - pos
 
 
-def tree_messages(n, r, G, iters, lag=1):
-    if is_leaf(n, r):  # sends nothing up: only the totals coming down
-        return [("dn", it, g) for it in range(iters) for g in range(G)]
+def role(t, n, r):
+    p = r if t == 0 else n - 1 - r
+    kids = [rank_at(t, n, c) for c in (2 * p + 1, 2 * p + 2) if c < n]
+    leaf_kids = [c < n and 2 * c + 1 >= n for c in (2 * p + 1, 2 * p + 2) if c < n]
+    root = p == 0
+    return {"pos": p, "root": root, "leaf": not root and not kids, "kids": kids, "leaf_kids": leaf_kids,
+            "parent": None if root else rank_at(t, n, (p - 1) // 2)}
+
+
+def tree_messages(n, r, G, iters, lag):
+    """The message sequence as specified: by time, ups then tree 0's downs
+    then tree 1's downs.  iters: tile iterations of each tree's part."""
+    R = [role(0, n, r), role(1, n, r)]
     seq = []
-    for it in range(iters + lag):
-        if it < iters:
-            for g in range(G):
-                seq.append(("up", it, g))
-        if it >= lag and r > 0:
-            for g in range(G):
-                seq.append(("dn", it - lag, g))
+    for time in range(max(iters) + lag):
+        for cls in range(4):
+            t, up = cls & 1, cls < 2
+            if up:
+                if R[t]["leaf"] or time >= iters[t]:
+                    continue
+                it = time
+            else:
+                if R[t]["root"] or time < lag or time - lag >= iters[t]:
+                    continue
+                it = time - lag
+            seq.extend((t, "up" if up else "dn", it, g) for g in range(G))
     return seq
 
 
 def cursor_sequence(n, r, G, iters, lag):
-    """The kernel's message cursor (TreeCursor) restated: after the up
-    messages of iteration it come the down messages of iteration it - lag;
-    once the ups are done, the remaining downs."""
-    root, leaf = r == 0, is_leaf(n, r)
-    Q = iters * G * (1 if root or leaf else 2)
-    it, ph, g = (lag, 1, 0) if leaf else (0, 0, 0)
+    """The kernel's cursor (TreeSeq, TreeCursor) restated: class c has
+    messages at the times [lo[c], hi[c]); from (t, cls) the next message is
+    the first class >= cls with messages at t, else the next time."""
+    R = [role(0, n, r), role(1, n, r)]
+    lo, hi = [0] * 4, [0] * 4
+    Q = 0
+    for t in range(2):
+        lo[t], hi[t] = 0, 0 if R[t]["leaf"] else iters[t]
+        lo[2 + t], hi[2 + t] = lag, lag if R[t]["root"] else lag + iters[t]
+        Q += (hi[t] - lo[t] + hi[2 + t] - lo[2 + t]) * G
+    tend = max(hi)
+    t, cls, g = 0, 0, 0
+
+    def seek(t, cls):
+        while t < tend:
+            for c in range(cls, 4):
+                if lo[c] <= t < hi[c]:
+                    return t, c
+            t, cls = t + 1, 0
+        return t, cls
+
+    t, cls = seek(t, cls)
     seq = []
     for _ in range(Q):
-        seq.append(("up", it, g) if ph == 0 else ("dn", it - lag, g))
+        seq.append((cls & 1, "up" if cls < 2 else "dn", t if cls < 2 else t - lag, g))
         g += 1
         if g < G:
             continue
         g = 0
-        if leaf:
-            it += 1
-            continue
-        if ph == 0 and not root and it >= lag:
-            ph = 1
-            continue
-        it += 1
-        if it >= iters:
-            it = max(it, lag)
-            ph = 1
-        else:
-            ph = 0
+        t, cls = seek(t, cls + 1)
     return seq
-
-
-def children(n, r):
-    return [c for c in (2 * r + 1, 2 * r + 2) if c < n]
 
 
 def run_model(n, G, K, D, P, iters, seed, lag=1):
     rnd = random.Random(seed)
     seqs = [tree_messages(n, r, G, iters, lag) for r in range(n)]
+    roles = [[role(0, n, r), role(1, n, r)] for r in range(n)]
     npl = min(P, D)
-    # per rank: ordinals of up / down messages received and sent
     info = []
     for r in range(n):
-        kids = children(n, r)
         rows = []
-        up_in = up_out = dn_in = dn_out = 0
-        for kind, it, g in seqs[r]:
-            m = {"kind": kind, "it": it, "g": g}
+        up_in = up_out = dn_out = 0
+        dn_in = [0, 0]
+        up_trees, dn_trees = set(), set()
+        for t, kind, it, g in seqs[r]:
+            R = roles[r][t]
+            m = {"tree": t, "kind": kind, "it": it, "g": g}
             if kind == "up":
-                m["up_in"] = up_in if kids else None  # same ordinal for both children
-                up_in += 1 if kids else 0
-                if r > 0:
+                m["up_in"] = up_in  # same ordinal for both children
+                up_in += 1
+                if not R["root"]:
                     m["up_out"] = up_out
                     up_out += 1
-                elif kids:
+                    up_trees.add(t)
+                elif R["kids"]:
                     m["dn_out"] = dn_out
                     dn_out += 1
+                    dn_trees.add(t)
             else:
-                m["dn_in"] = dn_in
-                dn_in += 1
-                if kids:
+                m["dn_in"] = dn_in[t]
+                dn_in[t] += 1
+                if R["kids"]:
                     m["dn_out"] = dn_out
                     dn_out += 1
+                    dn_trees.add(t)
             rows.append(m)
+        # one up link and one down head per rank are enough
+        assert len(up_trees) <= 1 and len(dn_trees) <= 1, (n, r, up_trees, dn_trees)
         info.append(rows)
     Q = [len(s) for s in seqs]
     X = [0] * n
@@ -144,11 +171,10 @@ def run_model(n, G, K, D, P, iters, seed, lag=1):
         return not ("up_out" in m and m["up_out"] >= K and up_tail[r] < m["up_out"] - K + 1)
 
     def data_ok(r, m):
+        R = roles[r][m["tree"]]
         if m["kind"] == "up":
-            if m["up_in"] is None:
-                return True
-            return all(up_head[c] >= m["up_in"] + 1 for c in children(n, r) if not is_leaf(n, c))
-        return dn_head[(r - 1) // 2] >= m["dn_in"] + 1
+            return all(up_head[c] >= m["up_in"] + 1 for c, lf in zip(R["kids"], R["leaf_kids"]) if not lf)
+        return dn_head[R["parent"]] >= m["dn_in"] + 1
 
     while True:
         acts = []
@@ -178,39 +204,38 @@ def run_model(n, G, K, D, P, iters, seed, lag=1):
         elif kind == "P":
             q = Pq[r][p]
             m = info[r][q]
-            if m["kind"] == "up" and m["up_in"] is not None:
+            R = roles[r][m["tree"]]
+            key = (m["tree"], m["it"], m["g"])
+            if m["kind"] == "up":
                 got = []
-                for c in children(n, r):
-                    if is_leaf(n, c):  # the leaf's input tile, there from the start
-                        got.append(((m["it"], m["g"]), ("x%d" % c,)))
+                for c, lf in zip(R["kids"], R["leaf_kids"]):
+                    if lf:  # the leaf's input tile, there from the start
+                        got.append((key, ("x%d" % c,)))
                         continue
                     sl = up_slots[c][m["up_in"] % K]
                     assert sl is not None and sl[0] == m["up_in"], ("up slot", r, q, c, sl)
                     got.append(sl[1])
                 stage[r][q % D] = got
-            elif m["kind"] == "dn":  # the parent's output, once posted
-                par = (r - 1) // 2
-                key = (m["it"], m["g"])
+            else:  # the parent's output, once posted
+                par = R["parent"]
                 assert key in out[par], ("output read before it was posted", r, q)
                 stage[r][q % D] = [(key, out[par][key])]
-            else:
-                stage[r][q % D] = []
             fullp[r][q % D] += 1
             Pq[r][p] += npl
         elif kind == "C":
             q = C[r]
             m = info[r][q]
-            key = (m["it"], m["g"])
+            R = roles[r][m["tree"]]
+            key = (m["tree"], m["it"], m["g"])
             got = stage[r][q % D]
-            kids = children(n, r)
             if m["kind"] == "up":
-                for k_, c in enumerate(kids):  # credits to the inner children
-                    if not is_leaf(n, c):
+                for c, lf in zip(R["kids"], R["leaf_kids"]):  # credits to the inner children
+                    if not lf:
                         up_tail[c] = max(up_tail[c], m["up_in"] + 1)
                 for v in got:
                     assert v[0] == key, ("wrong up message", v, key)
-                val = ("x%d" % r,) + tuple(v[1] for v in got)  # own, then left, then right
-                if r > 0:
+                val = ("x%d" % r,) + tuple(v[1] for v in got)  # own, then 2p+1's, then 2p+2's
+                if not R["root"]:
                     up_slots[r][m["up_out"] % K] = (m["up_out"], (key, val))
                 else:
                     out[r][key] = val
@@ -230,41 +255,52 @@ def run_model(n, G, K, D, P, iters, seed, lag=1):
                     dn_pub[r] += 1
             up_head[r], dn_head[r] = up_pub[r], dn_pub[r]
             S[r] = d
-    assert all(C[r] == Q[r] and S[r] == Q[r] for r in range(n)), ("deadlock", n, G, K, D, P)
+    assert all(C[r] == Q[r] and S[r] == Q[r] for r in range(n)), ("deadlock", n, G, K, D, P, iters)
 
-    def nested(r):
-        return ("x%d" % r,) + tuple(nested(c) for c in children(n, r))
+    def nested(t, p):
+        return ("x%d" % rank_at(t, n, p),) + tuple(nested(t, c) for c in (2 * p + 1, 2 * p + 2) if c < n)
 
-    want = nested(0)
     for r in range(n):
-        assert len(out[r]) == iters * G, (r, len(out[r]))
-        for key, v in out[r].items():
-            assert v == want, (r, key, v, want)
+        assert len(out[r]) == (iters[0] + iters[1]) * G, (r, len(out[r]))
+        for (t, it, g), v in out[r].items():
+            assert v == nested(t, 0), (r, t, it, g, v)
 
 
-CASES = [(n, G, K, D, P) for n in (1, 2, 3, 5, 8) for G, K in ((1, 2), (2, 3), (4, 8)) for D, P in ((1, 4), (2, 2), (3, 4))]
+CASES = [(n, G, K, D, P) for n in (2, 3, 5, 8) for G, K in ((1, 2), (2, 3), (4, 8)) for D, P in ((1, 4), (2, 2), (3, 4))]
 
 
 @pytest.mark.parametrize("n,G,K,D,P", CASES)
 def test_staged_tree_protocol(n, G, K, D, P):
     for seed in range(3):
-        run_model(n, G, K, D, P, iters=3, seed=seed)
+        run_model(n, G, K, D, P, iters=(3, 3), seed=seed)
 
 
 @pytest.mark.parametrize("lag", [2, 3, 5])
-@pytest.mark.parametrize("n,G,K,D,P", [(n, G, G + 1, D, P) for n in (2, 3, 5, 8) for G in (1, 2, 4)
+@pytest.mark.parametrize("n,G,K,D,P", [(n, G, G + 1, D, P) for n in (2, 3, 4, 5, 8) for G in (1, 2, 4)
                                        for D, P in ((1, 4), (2, 2), (3, 4))])
 def test_staged_tree_protocol_lag(n, G, K, D, P, lag):
     # the broadcast trailing the reduction by several iterations: still no
-    # deadlock with K = G + 1, including fewer iterations than the lag
-    for iters in (1, 2, 4, 7):
-        run_model(n, G, K, D, P, iters=iters, seed=iters, lag=lag)
+    # deadlock with K = G + 1, including fewer iterations than the lag and
+    # parts of unequal length (the second part may be a unit shorter, or
+    # empty)
+    for iters in ((1, 1), (2, 1), (4, 4), (7, 6), (1, 0)):
+        run_model(n, G, K, D, P, iters=iters, seed=sum(iters), lag=lag)
 
 
 @pytest.mark.parametrize("lag", [1, 2, 3])
 def test_cursor_matches_sequence(lag):
-    for n in (1, 2, 5, 8):
+    for n in (2, 3, 5, 8):
         for r in range(n):
             for G in (1, 3):
-                for iters in (1, 2, 3, 6):
+                for iters in ((1, 1), (2, 1), (3, 3), (6, 5), (1, 0)):
                     assert cursor_sequence(n, r, G, iters, lag) == tree_messages(n, r, G, iters, lag)
+
+
+@pytest.mark.parametrize("n", [2, 4, 6, 8])
+def test_even_n_every_rank_has_one_heavy_role(n):
+    # with n even every rank has children in exactly one tree and is a leaf
+    # of the other, so each CTA carries one heavy and one light role
+    for r in range(n):
+        R = [role(0, n, r), role(1, n, r)]
+        assert sum(1 for x in R if x["kids"]) == 1
+        assert sum(1 for x in R if x["leaf"]) == 1 or any(x["root"] for x in R)
