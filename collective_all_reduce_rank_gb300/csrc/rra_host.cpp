@@ -134,8 +134,32 @@ rra_status_t record(const char* call, int algo, int n, size_t count, int dt, int
 struct TuneEntry {
   int n, dt, log2b, algo;
 };
+// The alpha-beta prior fitted on the box (per type and schedule): a call
+// of S bytes per rank over n ranks takes alpha * syncs(n) + beta * n * S.
+struct PriorEntry {
+  int dt, algo;
+  double alpha_us, beta_us_per_mib;
+};
 std::vector<TuneEntry> g_tune;
+std::vector<PriorEntry> g_prior;
 std::mutex g_tune_mu;
+
+// Synchronizations of a schedule (the alpha count of the pages' model):
+// 2(n-1) ring steps, one for one-shot, two for two-shot, 2 ceil(log2 n)
+// for a tree.
+double sync_steps(int algo, int n) {
+  switch (algo) {
+    case RRA_ALGO_RING: return 2.0 * (n - 1);
+    case RRA_ALGO_ONE_SHOT: return 1.0;
+    case RRA_ALGO_TWO_SHOT: return 2.0;
+    case RRA_ALGO_TREE: {
+      int l = 0;
+      while ((1 << l) < n) ++l;
+      return 2.0 * std::max(1, l);
+    }
+    default: return 1e30;
+  }
+}
 
 int ceil_log2(size_t x) {
   int l = 0;
@@ -683,8 +707,8 @@ void rra_debug_skip_rank(int rank) { g_skip_rank.store(rank); }
 
 rra_algo_t rra_select_algo(int nranks, size_t bytes_per_rank, rra_dtype_t dtype) {
   if (nranks <= 1) return RRA_ALGO_ONE_SHOT;
+  std::lock_guard<std::mutex> lk(g_tune_mu);
   {
-    std::lock_guard<std::mutex> lk(g_tune_mu);
     const int lb = ceil_log2(std::max<size_t>(1, bytes_per_rank));
     int best_l = -1, best_a = -1;
     for (const TuneEntry& t : g_tune)
@@ -694,13 +718,24 @@ rra_algo_t rra_select_algo(int nranks, size_t bytes_per_rank, rra_dtype_t dtype)
       }
     if (best_a >= 0) return (rra_algo_t)best_a;
   }
-  // Prior: the alpha-beta model of the "Algorithms" section, with the
-  // traffic of one GPU.  There, the n ranks' peer reads of a unit are the
-  // same HBM bytes, so one-shot moves 2nS (every input read once, every
-  // output written once) -- the same beta term as two-shot and the ring --
-  // with one synchronization against two-shot's two and the ring's 2(n-1):
-  // one-shot at every size (the measured table agrees at every size swept).
-  (void)dtype;
+  // Prior: the alpha-beta model of the "Algorithms" section with alpha and
+  // beta fitted on this GPU (the "ab" lines of the tuning table): the
+  // schedule with the least alpha * syncs(n) + beta * n * S.
+  double best_t = 0;
+  int best = -1;
+  const double nS_mib = (double)nranks * (double)bytes_per_rank / (1024.0 * 1024.0);
+  for (const PriorEntry& p : g_prior) {
+    if (p.dt != (int)dtype) continue;
+    const double t = p.alpha_us * sync_steps(p.algo, nranks) + p.beta_us_per_mib * nS_mib;
+    if (best < 0 || t < best_t) {
+      best_t = t;
+      best = p.algo;
+    }
+  }
+  if (best >= 0) return (rra_algo_t)best;
+  // No measurement at all (no table loaded): the same model with one GPU's
+  // traffic, where the n ranks' peer reads of a unit are the same HBM bytes,
+  // so every schedule moves 2nS and one-shot has the fewest syncs.
   return RRA_ALGO_ONE_SHOT;
 }
 
@@ -708,11 +743,13 @@ rra_status_t rra_load_tuning(const char* path) {
   if (!path) {
     std::lock_guard<std::mutex> lk(g_tune_mu);
     g_tune.clear();
+    g_prior.clear();
     return RRA_SUCCESS;
   }
   FILE* f = std::fopen(path, "r");
   if (!f) return RRA_ERR_INVALID_ARG;
   std::vector<TuneEntry> t;
+  std::vector<PriorEntry> pr;
   char line[256];
   bool bad = false;
   while (std::fgets(line, sizeof line, f)) {
@@ -720,6 +757,18 @@ rra_status_t rra_load_tuning(const char* path) {
     if (hash) *hash = 0;
     char dts[32], al[32];
     int n = 0, lb = 0;
+    double alpha = 0, beta = 0;
+    if (std::sscanf(line, " ab %31s %31s %lf %lf", dts, al, &alpha, &beta) == 4) {
+      const int dt = !std::strcmp(dts, "int32") ? RRA_INT32 : !std::strcmp(dts, "float32") ? RRA_FLOAT32
+                     : !std::strcmp(dts, "bfloat16") ? RRA_BFLOAT16 : -1;
+      const int a = parse_algo(al);
+      if (dt < 0 || a < 0 || a == RRA_ALGO_DIRECT || !(alpha >= 0) || !(beta > 0)) {
+        bad = true;
+        break;
+      }
+      pr.push_back(PriorEntry{dt, a, alpha, beta});
+      continue;
+    }
     const int got = std::sscanf(line, "%d %31s %d %31s", &n, dts, &lb, al);
     if (got <= 0) continue;
     if (got != 4) { bad = true; break; }
@@ -736,6 +785,7 @@ rra_status_t rra_load_tuning(const char* path) {
   if (bad) return RRA_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_tune_mu);
   g_tune.swap(t);
+  g_prior.swap(pr);
   return RRA_SUCCESS;
 }
 
@@ -766,6 +816,10 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
             (env == RRA_ALGO_TREE && all_aligned16(bufs, nranks) && all_aligned16((const void* const*)outs, nranks)))
                ? (rra_algo_t)env
                : rra_select_algo(nranks, S, dtype);
+    // the tree moves 16-byte units by bulk copies: other buffers take
+    // one-shot, the schedule with the fewest syncs
+    if (algo == RRA_ALGO_TREE && !(all_aligned16(bufs, nranks) && all_aligned16((const void* const*)outs, nranks)))
+      algo = RRA_ALGO_ONE_SHOT;
   }
   if (count == 0) return record(call, algo, nranks, count, dtype, 0, RRA_SUCCESS);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -343,18 +343,23 @@ rra_status_t rra_query_status(rra_stream_t stream, int32_t info[4]);
 /** The schedule AUTO uses for an all-reduce of bytes_per_rank bytes per
  *  rank: from the measured table (rra_load_tuning; the table shipped
  *  beside the library is loaded by rra_init) when it has an entry for
- *  nranks and dtype, else from the alpha-beta cost model of [AIH]
- *  "Algorithms" with the traffic of one GPU, where the ranks' peer reads
- *  are the same HBM bytes: every schedule then moves the same 2nS bytes
- *  and one-shot has the fewest synchronizations, so the model gives
- *  one-shot at every size.  Never returns RRA_ALGO_AUTO. */
+ *  nranks and dtype; else from the alpha-beta cost model of [AIH]
+ *  "Algorithms" with alpha and beta fitted on this GPU (the table's "ab"
+ *  lines): the schedule with the least alpha * syncs(n) + beta * n * S,
+ *  syncs being 2(n-1) for the ring, 1 for one-shot, 2 for two-shot and
+ *  2 ceil(log2 n) for the tree; with no table loaded, one-shot (on one GPU
+ *  every schedule moves the same 2nS bytes and one-shot has the fewest
+ *  syncs).  AUTO never runs the tree on buffers that are not 16-byte
+ *  aligned.  Never returns RRA_ALGO_AUTO. */
 rra_algo_t rra_select_algo(int nranks, size_t bytes_per_rank, rra_dtype_t dtype);
 
 /** Load a tuning table ([AIH] "Algorithms": the alpha-beta crossovers are
  *  only illustrative and must be measured on one's own machine; this is
  *  where the measured ones go): text lines "nranks dtype log2_bytes algo"
- *  (dtype int32|float32|bfloat16, algo ring|one_shot|two_shot|tree); '#'
- *  starts a comment.  The entry with the largest log2_bytes <= ceil(log2(bytes))
+ *  (dtype int32|float32|bfloat16, algo ring|one_shot|two_shot|tree), and
+ *  prior lines "ab dtype algo alpha_us beta_us_per_MiB" (alpha per
+ *  synchronization, beta per MiB of nranks x bytes_per_rank); '#' starts a
+ *  comment.  The entry with the largest log2_bytes <= ceil(log2(bytes))
  *  for (nranks, dtype) wins.  NULL clears the table.  Errors:
  *  RRA_ERR_INVALID_ARG (unreadable or malformed file; the old table stays). */
 rra_status_t rra_load_tuning(const char* path);

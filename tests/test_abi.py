@@ -135,6 +135,35 @@ def test_selector_prior_and_tuning_table(lib, tmp_path):
     rra.rra_load_tuning(None)
 
 
+def test_fitted_alpha_beta_prior(lib, tmp_path):
+    """Where the table has no row for (n, dtype), the fitted alpha-beta
+    prior picks the schedule with the least alpha * syncs(n) + beta * n * S
+    (syncs: ring 2(n-1), one-shot 1, two-shot 2, tree 2 ceil(log2 n)).
+    With one-shot at alpha 1 us, beta 2 us per MiB of n*S and two-shot at
+    alpha 4 us (two syncs: 8 us), beta 1 us per MiB, one-shot is faster
+    while 1 + 2x < 8 + x, i.e. below x = n*S = 7 MiB."""
+    p = tmp_path / "prior.txt"
+    p.write_text("ab float32 one_shot 1.0 2.0\nab float32 two_shot 4.0 1.0\n"
+                 "ab float32 ring 100.0 1.0\n8 int32 10 ring\n")
+    rra.rra_load_tuning(str(p))
+    try:
+        # n = 4: x = 4 S / MiB; crossover at S = 7/4 MiB
+        assert rra.rra_select_algo(4, 1 << 20, rra.RRA_FLOAT32) == rra.RRA_ALGO_ONE_SHOT
+        assert rra.rra_select_algo(4, 2 << 20, rra.RRA_FLOAT32) == rra.RRA_ALGO_TWO_SHOT
+        # n = 7: crossover at S = 1 MiB
+        assert rra.rra_select_algo(7, (1 << 20) - 4096, rra.RRA_FLOAT32) == rra.RRA_ALGO_ONE_SHOT
+        assert rra.rra_select_algo(7, (1 << 20) + 4096, rra.RRA_FLOAT32) == rra.RRA_ALGO_TWO_SHOT
+        # the table's rows still win for their (n, dtype); other types fall
+        # back to one-shot with no prior of their own
+        assert rra.rra_select_algo(8, 1 << 10, rra.RRA_INT32) == rra.RRA_ALGO_RING
+        assert rra.rra_select_algo(8, 1 << 30, rra.RRA_BFLOAT16) == rra.RRA_ALGO_ONE_SHOT
+    finally:
+        rra.rra_load_tuning(None)
+    bad = tmp_path / "bad_prior.txt"
+    bad.write_text("ab float32 one_shot -1 2\n")
+    assert rra.rra_load_tuning(str(bad), check=False) == rra.RRA_ERR_INVALID_ARG
+
+
 def test_shipped_tuning_table(lib):
     # the table made by the size sweep on a GB300 loads, covers n = 2, 4, 8
     # for int32 and bfloat16 from 1 KiB to 1 GiB, and holds its one
