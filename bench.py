@@ -283,16 +283,36 @@ class Step:
         return sum(b for _, b, _, _ in self.ops)
 
 
-def check_parity_sample(step, oracle):
-    """A few sampled elements of every output against sums the oracle's
-    arithmetic gives for them (the full comparison lives in the tests)."""
-    rng = np.random.default_rng(1)
-    idx = rng.integers(0, step.count, size=64)
-    xs = step.host["bucket"]
-    sub = [np.ascontiguousarray(x[idx]) for x in xs]
-    want, _, _ = oracle.allreduce("oneshot", sub, "float32")
-    got = step.ar_out[3].cpu().numpy()[idx]
-    return bool(np.array_equal(got, want[0]))
+def check_consistency(torch, step, stream):
+    """Cross-schedule agreement on the bench's own outputs, without the
+    oracle (element-by-element parity with the oracle is what the tests
+    check): one-shot and two-shot sum every element in the same ascending
+    rank order, so their float32 results agree bit for bit on every rank;
+    the direct reduce-scatter's slice r is slice r of that sum; the direct
+    and ring all-gathers copy every shard unchanged.  Runs each operation
+    once more after the timed region."""
+    n, rc = N_RANKS, step.rc
+    with torch.cuda.stream(stream):
+        step.run_op("ar_oneshot", stream)
+    torch.cuda.synchronize()
+    one = [t.clone() for t in step.ar_out]
+    ok = True
+    for name in ("ar_twoshot",):
+        with torch.cuda.stream(stream):
+            step.run_op(name, stream)
+        torch.cuda.synchronize()
+        ok = ok and all(torch.equal(one[r], step.ar_out[r]) for r in range(n))
+    with torch.cuda.stream(stream):
+        step.run_op("rs_direct", stream)
+    torch.cuda.synchronize()
+    ok = ok and all(torch.equal(step.rs_out[r], one[r][r * rc:(r + 1) * rc]) for r in range(n))
+    for name in ("ag_direct", "ag_ring"):
+        with torch.cuda.stream(stream):
+            step.run_op(name, stream)
+        torch.cuda.synchronize()
+        ok = ok and all(torch.equal(step.ag_out[r][q * rc:(q + 1) * rc], step.sh[q])
+                        for r in range(n) for q in range(n))
+    return bool(ok)
 
 
 def run_ours(args):
@@ -365,9 +385,12 @@ def run_ours(args):
     h_sh = [torch.from_numpy(x).pin_memory() for x in step.host["shards"]]
     h_pl = [torch.from_numpy(p).pin_memory() for p in step.host["payloads"]]
 
+    # the step's results that come back: rank 0's output of every
+    # all-reduce and all-gather (identical on every rank), every rank's
+    # reduce-scatter slice (they differ), and both unpacked payloads
     def results(st_):
-        return (("ar", st_.ar_out[0]), ("rs", st_.rs_out[0]), ("ag", st_.ag_out[0]), ("ll", st_.ll_out),
-                ("l8", st_.l8_out))
+        return ((("ar", st_.ar_out[0]),) + tuple(("rs%d" % r, st_.rs_out[r]) for r in range(N_RANKS)) +
+                (("ag", st_.ag_out[0]), ("ll", st_.ll_out), ("l8", st_.l8_out)))
 
     h_res = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in results(step)}
     h2d = sum(t.numel() * t.element_size() for t in h_x + h_sh + h_pl)
@@ -423,9 +446,7 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError("device status after the end-to-end steps: %d %s" % (st, info))
 
-    import oracle
-
-    parity = check_parity_sample(step, oracle)
+    consistent = check_consistency(torch, step, stream)
 
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, "cuda")
     if rank != 0:
@@ -474,17 +495,19 @@ def run_ours(args):
         "ops": ops,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "returned": "rank 0's all-reduce and all-gather outputs (the same on every rank), every rank's "
+                            "reduce-scatter slice, both unpacked payloads",
                 "runs_ms": [round(x, 2) for x in e2e_runs], "of": "the median of five runs",
                 "overlap": "step k+1's inputs copy in and step k-1's results copy out while step k runs"},
         "gpu_launches": step.launches() * args.steps,
         "clocks": clk.summary(),
-        "parity_sample_ok": parity,
+        "consistency_ok": consistent,
     }
     if not args.no_next:
         line["next_rows"] = next_rows(torch, rra, inputs, step, stream)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_scale or 2)
-    if args.small:
+    if not args.no_small:
         line["tp_latency_us"] = tp_latency(torch, rra, inputs, stream)
     print(json.dumps(line), flush=True)
     if dist:
@@ -759,7 +782,12 @@ def run_reference(args):
 # --------------------------------------------------------------------------
 # tensor-parallel activations: small-message latency
 # --------------------------------------------------------------------------
-def tp_latency(torch, rra, inputs, stream, reps=200):
+def tp_latency(torch, rra, inputs, stream, reps=100):
+    """The tensor-parallel activations (n = 8, bfloat16 [t, 5120], t in
+    {1, 8, 32, 512}): microseconds per all-reduce for every schedule and
+    AUTO, from a CUDA graph of `reps` calls (the GPU's own time per call) and
+    from single launches between events (what one eager call costs, the
+    host's launch included), with algbw and busbw of the graph timing."""
     res = {}
     for t in inputs.TP_TOKENS:
         xs = inputs.cfg_tp_activations(t)
@@ -768,7 +796,8 @@ def tp_latency(torch, rra, inputs, stream, reps=200):
         S = t * inputs.TP_HIDDEN * 2
         row = {}
         for name, algo in (("ring", rra.RRA_ALGO_RING), ("oneshot", rra.RRA_ALGO_ONE_SHOT),
-                           ("twoshot", rra.RRA_ALGO_TWO_SHOT), ("auto", rra.RRA_ALGO_AUTO)):
+                           ("twoshot", rra.RRA_ALGO_TWO_SHOT), ("tree", rra.RRA_ALGO_TREE),
+                           ("auto", rra.RRA_ALGO_AUTO)):
             call = lambda: rra.rra_allreduce(ins, outs, t * inputs.TP_HIDDEN, rra.RRA_BFLOAT16,
                                              rra.RRA_SUM, algo, stream)
             with torch.cuda.stream(stream):
@@ -781,23 +810,119 @@ def tp_latency(torch, rra, inputs, stream, reps=200):
                     call()
             g.replay()
             torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            with torch.cuda.stream(stream):
-                g.replay()
-            b.record(stream)
-            torch.cuda.synchronize()
-            us = a.elapsed_time(b) * 1e3 / reps
+            samples = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                with torch.cuda.stream(stream):
+                    g.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                samples.append(a.elapsed_time(b) * 1e3 / reps)
+            us = statistics.median(samples)
+            single = []
+            for _ in range(20):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    call()
+                    b.record(stream)
+                torch.cuda.synchronize()
+                single.append(a.elapsed_time(b) * 1e3)
             alg = S / (us / 1e6) / 1e9
-            row[name] = {"us": round(us, 2), "algbw": round(alg, 1),
-                         "busbw": round(alg * 2 * (N_RANKS - 1) / N_RANKS, 1)}
+            row[name] = {"us": round(us, 2), "single_launch_us": round(statistics.median(single), 2),
+                         "algbw": round(alg, 1), "busbw": round(alg * 2 * (N_RANKS - 1) / N_RANKS, 1)}
         res["tokens=%d" % t] = row
     return res
 
 
 # --------------------------------------------------------------------------
+# LL / LL128 payload sweep (config 4)
+# --------------------------------------------------------------------------
+def run_ll_sweep(args):
+    """Pack (one source) and 4-source unpack-reduce of int32 payloads of
+    1 KiB .. 256 MiB in the LL and LL128 wire formats, flag = step counter:
+    floor GB/s (payload read + wire written for a pack; 4 wires read +
+    payload written for an unpack) and the fraction of the measured HBM peak
+    where the bytes exceed 4x the L2 (hot L2 below that)."""
+    import torch
+
+    import collective_all_reduce_rank_gb300 as rra
+    from collective_all_reduce_rank_gb300 import inputs
+
+    torch.cuda.set_device(0)
+    rra.rra_init(0)
+    stream = torch.cuda.Stream()
+    peak, _ = peaks()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    out = open(args.ll_sweep, "w")
+    flag = 0
+    for B in inputs.LL_SIZES:
+        ps = [torch.from_numpy(p).cuda() for p in inputs.cfg_ll_payloads(B, LL_SRC, seed=B)]
+        res = torch.empty(B // 4, dtype=torch.int32, device="cuda")
+        for fmt, wb, pack, unpack in (("ll", rra.rra_ll_wire_bytes(B), rra.rra_ll_pack, rra.rra_ll_unpack),
+                                      ("ll128", rra.rra_ll128_wire_bytes(B), rra.rra_ll128_pack,
+                                       rra.rra_ll128_unpack)):
+            wires = [torch.zeros(wb, dtype=torch.uint8, device="cuda") for _ in range(LL_SRC)]
+            flag += 1
+            f = flag
+            for p, w in zip(ps, wires):
+                pack(p, w, f, stream=stream)
+            torch.cuda.synchronize()
+            us_p, p10p, p90p = time_call(torch, lambda: pack(ps[0], wires[0], f, stream=stream), stream, B + wb)
+            us_u, p10u, p90u = time_call(torch, lambda: unpack(wires, res, f, stream=stream), stream,
+                                         LL_SRC * wb + B)
+            st, info = rra.rra_query_status(stream)
+            if st != 0:
+                raise SystemExit("device status %d %s at %s %d" % (st, info, fmt, B))
+            for op, us, p10, p90, fb in (("pack", us_p, p10p, p90p, B + wb),
+                                         ("unpack_reduce", us_u, p10u, p90u, LL_SRC * wb + B)):
+                gbs = fb / (us / 1e6) / 1e9
+                row = {"format": fmt, "op": op, "payload_bytes": B, "sources": LL_SRC if op != "pack" else 1,
+                       "wire_bytes": wb, "us": round(us, 3), "us_p10": round(p10, 3), "us_p90": round(p90, 3),
+                       "floor_bytes": fb, "GBps": round(gbs, 1), "frac_of_measured": round(gbs / peak, 3),
+                       "l2": "hot" if fb < 4 * l2 else "exceeds 4x L2"}
+                out.write(json.dumps(row) + "\n")
+                out.flush()
+                print(json.dumps(row), flush=True)
+        del ps, res
+        torch.cuda.empty_cache()
+    out.close()
+
+
+# --------------------------------------------------------------------------
 # message-size sweep (config 5) and the selector table
 # --------------------------------------------------------------------------
+SWEEP_DTYPES = ("int32", "bfloat16", "float32")
+
+
+def sync_steps(algo, n):
+    """Synchronizations a schedule needs (the alpha count of the pages'
+    alpha-beta model): 2(n-1) ring steps, one for one-shot, two for
+    two-shot, 2 ceil(log2 n) for a tree."""
+    return {"ring": 2 * (n - 1), "one_shot": 1, "two_shot": 2,
+            "tree": 2 * max(1, (n - 1).bit_length())}[algo]
+
+
+def fit_alpha_beta(rows):
+    """Per (dtype, schedule): t = alpha * sync_steps(n) + beta * n * S
+    fitted over every (n, S) point of the sweep by least squares on the
+    relative error (each point weighted by 1 / t, so microsecond and
+    millisecond calls count alike).  alpha in microseconds per
+    synchronization, beta in microseconds per MiB of n * S."""
+    fits = {}
+    keys = sorted({(r["dtype"], r["algo"]) for r in rows})
+    for dt, al in keys:
+        pts = [r for r in rows if r["dtype"] == dt and r["algo"] == al]
+        A = np.array([[sync_steps(al, r["n"]) / r["us"], r["n"] * r["bytes_per_rank"] / 2 ** 20 / r["us"]]
+                      for r in pts])
+        y = np.ones(len(pts))
+        coef, *_ = np.linalg.lstsq(A, y, rcond=None)
+        alpha, beta = max(0.0, float(coef[0])), max(1e-6, float(coef[1]))
+        fits[(dt, al)] = (alpha, beta)
+    return fits
+
+
 def run_sweep(args):
     import torch
 
@@ -809,35 +934,40 @@ def run_sweep(args):
     stream = torch.cuda.Stream()
     peak, _ = peaks()
     algos = (("ring", rra.RRA_ALGO_RING), ("one_shot", rra.RRA_ALGO_ONE_SHOT),
-             ("two_shot", rra.RRA_ALGO_TWO_SHOT))
+             ("two_shot", rra.RRA_ALGO_TWO_SHOT), ("tree", rra.RRA_ALGO_TREE))
     sizes = [s for s in inputs.SWEEP_SIZES if s <= args.sweep_max]
-    tune = []
+    tune, rows = [], []
     out = open(args.sweep, "w")
     # cold-L2 mode: a scratch buffer of twice the L2 size is rewritten
     # before every timed call
     l2_bytes = torch.cuda.get_device_properties(0).L2_cache_size
     flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device="cuda") if args.sweep_cold else None
+    codes = {"int32": rra.RRA_INT32, "bfloat16": rra.RRA_BFLOAT16, "float32": rra.RRA_FLOAT32}
     for n in inputs.SWEEP_RANKS:
-        for dtype in ("int32", "bfloat16"):
-            code = rra.RRA_INT32 if dtype == "int32" else rra.RRA_BFLOAT16
-            tdt = torch.int32 if dtype == "int32" else torch.bfloat16
-            e = 4 if dtype == "int32" else 2
+        for dtype in SWEEP_DTYPES:
+            code = codes[dtype]
             for S in sizes:
-                count = S // e
-                g = torch.Generator(device="cuda").manual_seed(S + n)
-                if dtype == "int32":
-                    ins = [torch.randint(-(1 << 20), (1 << 20) + 1, (count,), dtype=tdt, device="cuda",
-                                         generator=g) for _ in range(n)]
+                # the seeded numpy recipe of the sweep (the tests check the
+                # largest size per rank count and type against the oracle)
+                xs = inputs.cfg_sweep(n, S, dtype, seed=S + n)
+                count = xs[0].size
+                if dtype == "bfloat16":
+                    ins = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
                 else:
-                    ins = [torch.randn(count, device="cuda", generator=g).to(tdt) for _ in range(n)]
+                    ins = [torch.from_numpy(x).cuda() for x in xs]
+                del xs
                 outs = [torch.empty_like(x) for x in ins]
-                best = None
+                best, results = None, {}
                 for name, algo in algos:
                     call = lambda: rra.rra_allreduce(ins, outs, count, code, rra.RRA_SUM, algo, stream)
                     if flush is None:
                         us, p10, p90 = time_call(torch, call, stream, S * n)
                     else:
                         us, p10, p90 = time_call_cold(torch, call, stream, flush, S * n)
+                    st, info = rra.rra_query_status(stream)
+                    if st != 0:
+                        raise SystemExit("device status %d %s at n=%d %s %d %s" % (st, info, n, dtype, S, name))
+                    results[name] = [o.clone() for o in outs] if S * n <= (1 << 30) else [outs[0].clone()]
                     fb = 2 * n * S
                     alg = S / (us / 1e6) / 1e9
                     row = {"n": n, "dtype": dtype, "bytes_per_rank": S, "algo": name, "us": round(us, 3),
@@ -847,18 +977,32 @@ def run_sweep(args):
                            "pct_hbm_8TBps": round(100 * fb / (us / 1e6) / 1e9 / HBM_NOMINAL, 1),
                            "frac_of_measured": round(fb / (us / 1e6) / 1e9 / peak, 3),
                            "l2_resident": 2 * n * S < 4 * l2_bytes, "l2": "cold" if flush is not None else "hot"}
-                    out.write(json.dumps(row) + "\n")
-                    out.flush()
+                    rows.append(row)
                     if best is None or us < best[1]:
                         best = (name, us)
+                # consistency without the oracle: int32 sums are exact, so
+                # every schedule agrees bit for bit; one-shot and two-shot
+                # share the ascending order in every type
+                same = lambda a, b: all(torch.equal(x, y) for x, y in zip(a, b))
+                ok = same(results["one_shot"], results["two_shot"])
+                if dtype == "int32":
+                    ok = ok and all(same(results["one_shot"], results[k]) for k in results)
+                for row in rows[-len(algos):]:
+                    row["consistent"] = bool(ok)
+                    out.write(json.dumps(row) + "\n")
+                out.flush()
                 tune.append((n, dtype, (S - 1).bit_length(), best[0]))
-                del ins, outs
+                del ins, outs, results
                 torch.cuda.empty_cache()
     out.close()
+    fits = fit_alpha_beta(rows)
     with open(args.sweep + ".tune.txt", "w") as f:
         f.write("# nranks dtype log2_bytes algo  (fastest measured schedule per size)\n")
         for n, dtype, lb, name in tune:
             f.write("%d %s %d %s\n" % (n, dtype, lb, name))
+        f.write("# ab dtype algo alpha_us_per_sync beta_us_per_MiB_of_nS  (fitted over the sweep)\n")
+        for (dt, al), (alpha, beta) in sorted(fits.items()):
+            f.write("ab %s %s %.4f %.6f\n" % (dt, al, alpha, beta))
 
 
 def spread(samples):
@@ -941,13 +1085,34 @@ def run_profile(args):
     stream = torch.cuda.Stream()
     names = [o[0] for o in step.ops] if args.profile == "all" else args.profile.split(",")
     step.flag = 1
+    extra = {}
+    if "ar_ring_bf16" in names:
+        # bfloat16 ring on as many bytes per rank as the float32 bucket
+        xs = inputs.make_ranks(N_RANKS, 2 * step.count, "bfloat16", "normal", seed=5)
+        extra["bf16_in"] = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
+        extra["bf16_out"] = [torch.empty_like(t) for t in extra["bf16_in"]]
+    if "ar_rmsnorm" in names:
+        # tensor-parallel activations [rows, 5120] bfloat16, rows so that the
+        # 8 ranks' inputs exceed L2
+        rows = 4096
+        xs = inputs.make_ranks(N_RANKS, rows * inputs.TP_HIDDEN, "bfloat16", "normal", seed=6)
+        extra["tp_in"] = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
+        extra["tp_out"] = [torch.empty_like(t) for t in extra["tp_in"]]
+        extra["gamma"] = torch.ones(inputs.TP_HIDDEN, dtype=torch.bfloat16, device="cuda")
     with torch.cuda.stream(stream):
         for name in names:
             if name == "ll_unpack" and "ll_pack" not in names:
                 step.run_op("ll_pack", stream)
             if name == "ll128_unpack" and "ll128_pack" not in names:
                 step.run_op("ll128_pack", stream)
-            step.run_op(name, stream)
+            if name == "ar_ring_bf16":
+                rra.rra_allreduce(extra["bf16_in"], extra["bf16_out"], 2 * step.count, rra.RRA_BFLOAT16,
+                                  rra.RRA_SUM, rra.RRA_ALGO_RING, stream)
+            elif name == "ar_rmsnorm":
+                rra.rra_allreduce_rmsnorm(extra["tp_in"], extra["tp_out"], extra["gamma"], inputs.TP_HIDDEN,
+                                          1e-6, stream=stream)
+            else:
+                step.run_op(name, stream)
     torch.cuda.synchronize()
     st, info = rra.rra_query_status(stream)
     if st != 0:
@@ -969,7 +1134,9 @@ def main():
     ap.add_argument("--scale", type=int, default=4, help="workload fraction for --profile")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the rows beyond the step (tree, RMSNorm, ...)")
-    ap.add_argument("--small", action="store_true", help="add the TP-activation latency table")
+    ap.add_argument("--no-small", action="store_true", help="skip the TP-activation latency table")
+    ap.add_argument("--ll-sweep", default=None,
+                    help="write the LL / LL128 payload sweep (1 KiB .. 256 MiB, 4 sources) to this JSONL file")
     ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")
     ap.add_argument("--sweep-max", type=int, default=1 << 30)
     ap.add_argument("--sweep-cold", action="store_true",
@@ -983,6 +1150,8 @@ def main():
         run_profile(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.ll_sweep:
+        run_ll_sweep(args)
     else:
         run_ours(args)
 
