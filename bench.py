@@ -837,6 +837,60 @@ def tp_latency(torch, rra, inputs, stream, reps=100):
 
 
 # --------------------------------------------------------------------------
+# the ring's link forms against size (the protocol crossover)
+# --------------------------------------------------------------------------
+def run_ring_forms(args):
+    """The ring all-reduce per size in its default form (the one the
+    library picks by size) and forced into the staged form (Simple links)
+    and the per-warp LL form: n = 2, 4, 8, fp32 and bf16, 1 KiB .. 16 MiB per
+    rank, a CUDA graph of 50 calls per point (hot L2).  The forms must agree
+    bit for bit (the same ring order); a point where they do not, or where a
+    wait expired, stops the run."""
+    import torch
+
+    import collective_all_reduce_rank_gb300 as rra
+    from collective_all_reduce_rank_gb300 import inputs
+
+    torch.cuda.set_device(0)
+    rra.rra_init(0)
+    stream = torch.cuda.Stream()
+    out = open(args.ring_forms, "w")
+    for dtype, code in (("float32", rra.RRA_FLOAT32), ("bfloat16", rra.RRA_BFLOAT16)):
+        for n in inputs.SWEEP_RANKS:
+            for k in range(10, 25):
+                S = 1 << k
+                xs = inputs.cfg_sweep(n, S, dtype, seed=S + n)
+                count = xs[0].size
+                if dtype == "bfloat16":
+                    ins = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
+                else:
+                    ins = [torch.from_numpy(x).cuda() for x in xs]
+                outs = [torch.empty_like(x) for x in ins]
+                call = lambda: rra.rra_allreduce(ins, outs, count, code, rra.RRA_SUM, rra.RRA_ALGO_RING, stream)
+                row = {"dtype": dtype, "n": n, "bytes_per_rank": S}
+                row["default_us"], _, _ = time_call(torch, call, stream, 0)
+                ref = [o.clone() for o in outs]
+                for form in ("staged", "ll"):
+                    os.environ["RRA_RING_PROTO"] = form
+                    try:
+                        row[form + "_us"], _, _ = time_call(torch, call, stream, 0)
+                    finally:
+                        os.environ.pop("RRA_RING_PROTO")
+                    if not all(torch.equal(a, b) for a, b in zip(ref, outs)):
+                        raise SystemExit("ring forms disagree at n=%d %s %d (%s)" % (n, dtype, S, form))
+                st, info = rra.rra_query_status(stream)
+                if st != 0:
+                    raise SystemExit("device status %d %s" % (st, info))
+                for key in ("default_us", "staged_us", "ll_us"):
+                    row[key] = round(row[key], 2)
+                row["fastest"] = min(("staged", "ll"), key=lambda f: row[f + "_us"])
+                out.write(json.dumps(row) + "\n")
+                out.flush()
+                print(json.dumps(row), flush=True)
+    out.close()
+
+
+# --------------------------------------------------------------------------
 # LL / LL128 payload sweep (config 4)
 # --------------------------------------------------------------------------
 def run_ll_sweep(args):
@@ -1135,6 +1189,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the rows beyond the step (tree, RMSNorm, ...)")
     ap.add_argument("--no-small", action="store_true", help="skip the TP-activation latency table")
+    ap.add_argument("--ring-forms", default=None,
+                    help="write the ring's default, staged and LL forms against size to this JSONL file")
     ap.add_argument("--ll-sweep", default=None,
                     help="write the LL / LL128 payload sweep (1 KiB .. 256 MiB, 4 sources) to this JSONL file")
     ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")
@@ -1152,6 +1208,8 @@ def main():
         run_sweep(args)
     elif args.ll_sweep:
         run_ll_sweep(args)
+    elif args.ring_forms:
+        run_ring_forms(args)
     else:
         run_ours(args)
 

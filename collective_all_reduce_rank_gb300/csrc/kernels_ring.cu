@@ -122,7 +122,11 @@ struct RingWarp {
         if (consumed) st_relaxed(tail_in, E | (uint64_t)(m_in + 1));
       }
     } else if (lane == 0) {
-      if (consumed && ((m_in + 1) % (uint32_t)a.G) == 0) st_release(tail_in, E | (uint64_t)(m_in + 1));
+      // a credit is a release (the slot's lines were read before it); a
+      // call too short to reuse any slot needs none, which takes the
+      // release off every hop of a small message
+      if (consumed && !a.no_credits && ((m_in + 1) % (uint32_t)a.G) == 0)
+        st_release(tail_in, E | (uint64_t)(m_in + 1));
       // progress marker only (the lines carry their own flags): lets a peer
       // that gives up tell a rank that never sent from one stuck behind it
       if (sent && ((m_out + 1) % (uint32_t)a.G) == 0) st_relaxed(head_out, E | (uint64_t)(m_out + 1));

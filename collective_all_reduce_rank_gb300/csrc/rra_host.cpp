@@ -307,19 +307,35 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
   return cuda_status(launch_twoshot(n, dt, vec, a, n * (int)c, st));
 }
 
-// The ring's form.  RRA_RING_PROTO=ll | simple | staged forces one.  By
-// default the staged form (measured fastest at every size on GB300: 40 us
-// against 46 us for LL at 1 KiB x 8 ranks, 78 us against 262 us at 8 MiB);
-// it needs 16-byte aligned buffers and chunk starts, and without them the
-// per-warp LL form takes chunks up to RRA_RING_LL_MAX_BYTES (64 KiB) and
-// the per-warp Simple form larger ones.
+// The ring's form, by measured size ([AIH] "Protocols": LL for small
+// messages, Simple for large ones).  RRA_RING_PROTO=ll | simple | staged
+// forces one.  On 16-byte aligned buffers the staged form (Simple links,
+// whole-CTA messages) is the fastest for large chunks and at 2 ranks (where
+// its first message needs no hop); the per-warp LL form for small and
+// mid-size chunks at 4 ranks and more, where both are bound by the ring's
+// 2(n-1) hops and an LL hop is the cheaper (CUDA graph of 50 calls): fp32 at
+// 8 ranks 28 against 39 us at 1-4 KiB per rank, 34.5 against 40.6 at
+// 32 KiB, 40.0 against 44.3 at 1 MiB, 44.7 against 46.5 at 2 MiB, then
+// slower (95 against 51 at 4 MiB); at 4 ranks 14.7 against 18.6 at 1-2 KiB,
+// 17.5 against 19.4 at 16-32 KiB, a tie from 64 KiB to 1 MiB; bf16, whose
+// LL lines carry fp32 partials, to 32 KiB per rank at 8 ranks and 2 KiB at 4.
+// So LL takes chunks up to 256 KiB (bf16 4 KiB) at n >= 8 and up to 8 KiB
+// (bf16 512 B) at 4 <= n < 8; RRA_RING_LL_STAGED_MAX_BYTES overrides the
+// limit.  Without 16-byte alignment the per-warp LL form takes chunks up to
+// RRA_RING_LL_MAX_BYTES (64 KiB) and the per-warp Simple form larger ones.
 enum RingForm { kFormWarpSimple = 0, kFormWarpLL = 1, kFormStaged = 2 };
 
-int ring_form(size_t chunk_bytes, bool staged_ok) {
+int ring_form(size_t chunk_bytes, bool staged_ok, int n, rra_dtype_t dt) {
   const char* p = std::getenv("RRA_RING_PROTO");
   if (p && !std::strcmp(p, "simple")) return kFormWarpSimple;
   if (p && !std::strcmp(p, "ll")) return kFormWarpLL;
-  if (staged_ok) return kFormStaged;
+  if (p && !std::strcmp(p, "staged") && staged_ok) return kFormStaged;
+  if (staged_ok) {
+    static const long ll_max = env_long("RRA_RING_LL_STAGED_MAX_BYTES", -1);
+    const long lim = ll_max >= 0 ? ll_max
+                     : dt == RRA_BFLOAT16 ? (n >= 8 ? 4096L : 512L) : (n >= 8 ? 256L << 10 : 8192L);
+    return (n >= 4 && (long)chunk_bytes <= lim) ? kFormWarpLL : kFormStaged;
+  }
   static const long limit = env_long("RRA_RING_LL_MAX_BYTES", 64L << 10);
   return (long)chunk_bytes <= limit ? kFormWarpLL : kFormWarpSimple;
 }
@@ -334,10 +350,14 @@ static size_t staged_smem_budget() {
 }
 
 // Staged ring: messages of T units, G per step, K slots per link, D stages.
-// Defaults (measured on GB300, 8 ranks x 100 MB per rank): G = 6, T up to
-// 2048 units for 4-byte types and up to 1536 for bfloat16 (whose partials
-// travel as float32); K = 2G.  Larger G fills L2 with FIFO
-// slots (links x K x slot bytes) and runs slower.  Channels: as many as the GPU holds, but no more than
+// Defaults (measured on GB300, 8 ranks x 100 MB per rank, T x G x K sweep):
+// G = 6; T up to 2368 units for 4-byte types and up to 1536 for bfloat16
+// (whose partials travel as float32), the largest tiles that still leave
+// three stages (T 2304 with three stages: 0.347 ms; T 1728 with four:
+// 0.364; T 2592 with two: 0.45); K = G + 3 (K = 2G keeps 1.3x the FIFO
+// slots in L2 and measured 2-3% slower, K = G + 1 stalls on credits).
+// Larger G fills L2 with FIFO slots (links x K x slot bytes) and runs
+// slower.  Channels: as many as the GPU holds, but no more than
 // leave G tiles of 128 units each; then T is the smallest multiple of 32
 // units that covers the chunk in whole iterations, so no iteration runs
 // nearly empty.  K drops to G + 1 when the FIFO would not fit the workspace.
@@ -345,11 +365,26 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
                              int* grid_out) {
   const int n = a.n;
   const size_t aw = dt == RRA_BFLOAT16 ? 2 : 1;
-  // G: the default, or fewer when the chunk fills fewer than G tiles of 128
-  // units per channel (every message of a step costs a hop, even empty)
-  const size_t gfill = (maxu + (size_t)s->sms / n * 128 - 1) / std::max<size_t>(1, (size_t)s->sms / n * 128);
-  a.G = (int)std::max(1L, env_long("RRA_RING_G", std::min<long>(6, (long)std::max<size_t>(1, gfill))));
-  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_RING_TILE", aw == 2 ? 1536 : 2048)));
+  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_RING_TILE", aw == 2 ? 1536 : 2368)));
+  // G, messages per step, by the units u each channel carries of a chunk,
+  // as measured best on GB300 (n = 4 and 8, fp32 and bf16, 128 KiB .. 16 MiB
+  // per rank, G = 1 .. 8: every pick within 2% of the best): one message per
+  // step while a step's message is small (u < 600), so no hop waits on
+  // several; then 2 and 3, which let the next rank start on a step's first
+  // messages; from 2600 units 4, as long as four messages cover the chunk in
+  // one iteration, else 6 (more iterations: the messages of a step hide the
+  // hop).  The old rule (up to 6 whenever 6 tiles of 128 units filled a
+  // channel) was 10-35% slower from 1 to 16 MiB per rank.
+  {
+    const size_t ch_est = std::max<size_t>(1, (size_t)s->sms / n);
+    const size_t u = (maxu + ch_est - 1) / ch_est;
+    long g = 6;
+    if (u < 600) g = 1;
+    else if (u < 1300) g = 2;
+    else if (u < 2600) g = 3;
+    else if (u <= 4 * (size_t)tmax) g = 4;
+    a.G = (int)std::max(1L, env_long("RRA_RING_G", g));
+  }
   auto stages_for = [&](long t) {
     const long d = (long)(staged_smem_budget() / ((size_t)t * 16 * (1 + aw)));
     return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_RING_STAGES", 8)}));
@@ -371,7 +406,7 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
   err = ring_staged_occupancy(dt, (int)T, a.stages, &occ);
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   a.slot_bytes = (size_t)T * 16 * aw;
-  a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", 2L * a.G));
+  a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", (long)a.G + 3));
   if ((size_t)c * n * a.K * a.slot_bytes > s->ws.fifo_bytes) a.K = a.G + 1;
   c = std::min<long>(c, (long)(s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes)));
   if (c < 1) return RRA_ERR_WORKSPACE;
@@ -514,7 +549,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   }
   bool staged_ok = vec;
   for (int c = 0; c < n; ++c) staged_ok = staged_ok && (ibase[c] * e) % 16 == 0 && (obase[c] * e) % 16 == 0;
-  const int form = ring_form(maxu * 16, staged_ok);
+  const int form = ring_form(maxu * 16, staged_ok, n, dt);
   if (form == kFormStaged) return run_ring_staged(s, a, maxu, dt, st, grid_out);
   const int proto = form == kFormWarpLL ? kProtoLL : kProtoSimple;
   a.slice_units = kRingThreads * kRingUnitsPerThread;
@@ -570,6 +605,13 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   a.head = s->ws.flags;
   a.tail = s->ws.flags + kLinkFlags;
   a.wait = wait_cfg(s);
+  if (proto == kProtoLL) {
+    // messages per link in this call; with no more than K, no slot is
+    // reused and no sender waits for a credit
+    const size_t iters = (maxu + (size_t)c * a.G * a.slice_units - 1) / ((size_t)c * a.G * a.slice_units);
+    const size_t sends = mode == kRingAllReduce ? 2 * (size_t)(n - 1) : (size_t)(n - 1);
+    a.no_credits = iters * sends * (size_t)a.G <= (size_t)a.K ? 1 : 0;
+  }
   *grid_out = n * (int)c;
   return cuda_status(launch_ring(dt, vec, proto, a, n * (int)c, st));
 }

@@ -112,6 +112,8 @@ struct RingArgs {
   int G;            // messages per step and iteration
   int K;            // FIFO slots per link
   int stages;       // staged form: shared-memory stages per CTA
+  int no_credits;   // per-warp LL form: no slot is reused in this call, so
+                    // receivers raise no credits (the sender never waits)
   WaitCfg wait;
 };
 

@@ -55,14 +55,20 @@
  *                        rra_set_max_ctas() sets one
  *   RRA_DEBUG            1: print each call (schedule, grid, status) and
  *                        every CUDA error to stderr
- *   RRA_RING_PROTO       ring links for every buffer: staged (default when
- *                        16-byte aligned), simple or ll (per-warp forms)
- *   RRA_RING_LL_MAX_BYTES  largest chunk the per-warp ring sends as LL
- *                        lines (64 KiB; larger ones use Simple)
+ *   RRA_RING_PROTO       ring links for every buffer: staged, simple or ll
+ *                        (per-warp forms); default by size (below)
+ *   RRA_RING_LL_STAGED_MAX_BYTES  on 16-byte aligned buffers with 4 ranks
+ *                        or more, chunks up to this many bytes take LL
+ *                        lines (measured faster there; default 256 KiB at 8
+ *                        ranks and 8 KiB below, bfloat16 4 KiB and 512 B),
+ *                        larger ones the staged form
+ *   RRA_RING_LL_MAX_BYTES  on other buffers, the largest chunk the per-warp
+ *                        ring sends as LL lines (64 KiB; larger: Simple)
  *   RRA_RING_CLUSTER     1: the ring on thread-block clusters
  *   RRA_RING_TILE, RRA_RING_G, RRA_RING_K, RRA_RING_STAGES,
- *   RRA_RING_CHANNELS    staged ring: units per message (<= 2048, 1536 for
- *                        bfloat16), messages per step (6), FIFO slots (2G),
+ *   RRA_RING_CHANNELS    staged ring: units per message (<= 2368, 1536 for
+ *                        bfloat16), messages per step (1-6 by the chunk's
+ *                        size per channel), FIFO slots (G+3),
  *                        shared-memory stages, CTAs per rank
  *   RRA_STAGED_SMEM_KB   shared memory for the staged ring's and tree's
  *                        stages (224)
