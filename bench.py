@@ -1145,6 +1145,11 @@ def run_profile(args):
         xs = inputs.make_ranks(N_RANKS, 2 * step.count, "bfloat16", "normal", seed=5)
         extra["bf16_in"] = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
         extra["bf16_out"] = [torch.empty_like(t) for t in extra["bf16_in"]]
+    if "ar_twoshot_n2" in names or "ar_oneshot_n2" in names:
+        # two ranks of 64 MiB fp32 (256 MiB in and out: past L2)
+        xs = inputs.make_ranks(2, (64 << 20) // 4, "float32", "normal", seed=7)
+        extra["n2_in"] = [torch.from_numpy(x).cuda() for x in xs]
+        extra["n2_out"] = [torch.empty_like(t) for t in extra["n2_in"]]
     if "ar_rmsnorm" in names:
         # tensor-parallel activations [rows, 5120] bfloat16, rows so that the
         # 8 ranks' inputs exceed L2
@@ -1162,6 +1167,10 @@ def run_profile(args):
             if name == "ar_ring_bf16":
                 rra.rra_allreduce(extra["bf16_in"], extra["bf16_out"], 2 * step.count, rra.RRA_BFLOAT16,
                                   rra.RRA_SUM, rra.RRA_ALGO_RING, stream)
+            elif name in ("ar_twoshot_n2", "ar_oneshot_n2"):
+                algo = rra.RRA_ALGO_TWO_SHOT if name == "ar_twoshot_n2" else rra.RRA_ALGO_ONE_SHOT
+                rra.rra_allreduce(extra["n2_in"], extra["n2_out"], extra["n2_in"][0].numel(), rra.RRA_FLOAT32,
+                                  rra.RRA_SUM, algo, stream)
             elif name == "ar_rmsnorm":
                 rra.rra_allreduce_rmsnorm(extra["tp_in"], extra["tp_out"], extra["gamma"], inputs.TP_HIDDEN,
                                           1e-6, stream=stream)

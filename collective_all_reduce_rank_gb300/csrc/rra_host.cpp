@@ -444,7 +444,15 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   const size_t h = std::min(count, ((count + 1) / 2 + pu - 1) / pu * pu);
   a.half_units = (h + pu - 1) / pu;
   const size_t part = std::max(a.half_units, units - a.half_units);  // units of the larger part
-  a.G = (int)std::max(1L, env_long("RRA_TREE_G", 24));
+  // G tiles per iteration (24 for the bucket), but no more than the part
+  // fills with tiles of 128 units per channel: every message of a role
+  // costs a synchronization even when it carries nothing, and a small
+  // message is one up-and-back wave
+  {
+    const size_t ch_est = std::max<size_t>(1, (size_t)s->sms / n);
+    const size_t fill = (part + ch_est * 128 - 1) / (ch_est * 128);
+    a.G = (int)std::max(1L, env_long("RRA_TREE_G", (long)std::max<size_t>(1, std::min<size_t>(24, fill))));
+  }
   a.lag = (int)std::max(1L, std::min(64L, env_long("RRA_TREE_LAG", aw == 2 ? 4 : 6)));
   const long tmax = std::max(64L, std::min(4096L, env_long("RRA_TREE_TILE", aw == 2 ? 1024 : 2048)));
   auto stages_for = [&](long t) {
