@@ -42,7 +42,8 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
                                              int W, uint64_t E, uint32_t tag) {
   constexpr int PU = Elem<DT>::kPerUnit;
   constexpr int ES = Elem<DT>::kSize;
-  constexpr int F = twoshot_lag<N>();
+  // the measured default, or the host's (RRA_TWOSHOT_LAG)
+  const size_t F = a.lag > 0 ? (size_t)a.lag : (size_t)twoshot_lag<N>();
   constexpr int UPT = twoshot_units_per_thread(N);  // units per lane per tile
   constexpr int NY = N > 1 ? N - 1 : 1;
   const int C = a.channels;
@@ -74,7 +75,7 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
 
   for (size_t it = 0; it < iters + F; ++it) {
     // 1. gather loads of tile gi = it - F
-    const bool gather = it >= (size_t)F;
+    const bool gather = it >= F;
     const size_t gi = it - F;
     uint4 y[UPT][NY];
     int vy[UPT][NY];

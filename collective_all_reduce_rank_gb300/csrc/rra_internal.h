@@ -87,6 +87,7 @@ struct TwoShotArgs {
   uint64_t* progress;           // [(rank * channels + ch) * warps + warp]
   int channels;
   int tile_units;  // 16-byte units per tile per iteration
+  int lag;         // tiles the gather trails the reduce by (0: the measured default)
   WaitCfg wait;
 };
 

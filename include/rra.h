@@ -79,6 +79,9 @@
  *                        reduction (6, 4 for bfloat16), stages, CTAs per rank
  *   RRA_TWOSHOT_CLUSTER  1: two-shot on thread-block clusters
  *   RRA_TWOSHOT_CHANNELS CTAs per rank of two-shot
+ *   RRA_TWOSHOT_LAG      tiles the two-shot's gather trails its reduce by
+ *                        (and between its progress flags): 16 at 8 ranks, 8
+ *                        below
  *   RRA_ONESHOT_TMA      1: one-shot with bulk copies through shared memory
  *   RRA_ONESHOT_PER_RANK 1: one-shot reads the n inputs once per rank, as
  *                        n GPUs would (out of place only; in place keeps
