@@ -8,8 +8,8 @@
 //
 // One persistent cooperative launch of n x C CTAs.  CTA (r, ch) is channel
 // ch of virtual rank r; its 16 warps are independent pipelines, each lane
-// with 8/n (at least 1) 16-byte units per tile so that n sources keep
-// about the same bytes in flight.  Warp w handles its part of tile t of
+// with 2 (two ranks) or 1 16-byte units per tile; up to four ranks two CTAs
+// share an SM.  Warp w handles its part of tile t of
 // every chunk in turn and, in trip i of its loop,
 //   1. issues the loads of the all-gather part of tile i - F: the other
 //      ranks' sums, from outs[q] (L2), after acquiring their progress;
@@ -139,7 +139,7 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
 }
 
 template <int N, int DT, bool VEC>
-__global__ void __launch_bounds__(kDirectThreads, 1) twoshot_kernel(const __grid_constant__ TwoShotArgs a) {
+__global__ void __launch_bounds__(kDirectThreads, twoshot_min_blocks(N)) twoshot_kernel(const __grid_constant__ TwoShotArgs a) {
   __shared__ uint32_t s_epoch;
   if (threadIdx.x == 0) s_epoch = read_epoch(a.wait.sync);
   __syncthreads();

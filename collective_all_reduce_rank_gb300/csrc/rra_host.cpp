@@ -297,8 +297,11 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   const size_t units0 = (a.chunk_len[0] + pu - 1) / pu;
   const size_t need = (units0 + a.tile_units - 1) / a.tile_units;
-  long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
-                           channel_cap(n)});
+  // enough channels to fill every SM at the kernel's CTAs per SM, within the
+  // progress words (one per rank, channel and warp) and the SM budget
+  const long words_cap = (long)(kLinkFlags / ((size_t)n * kMaxWarps));
+  const long budget_cap = rra::max_ctas_cap() > 0 ? channel_cap(n) : words_cap;
+  long c = std::min<long>({words_cap, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need), budget_cap});
   c = std::min(c, env_long("RRA_TWOSHOT_CHANNELS", c));
   if (c < 1) return RRA_ERR_UNSUPPORTED;
   a.channels = (int)c;
@@ -424,12 +427,15 @@ rra_status_t run_ring_staged(DevState* s, RingArgs& a, size_t maxu, rra_dtype_t 
 
 // Staged double binary tree: the message split in two by the chunk plan for
 // two parts (the first part on tree 0, the rest on tree 1); one message per
-// tile of T units (T <= RRA_TREE_TILE: 2048 for 4-byte types, 1024 for
+// tile of T units (T <= RRA_TREE_TILE: 2048 for 4-byte types, 1280 for
 // bfloat16, whose partials travel as float32), G tiles per iteration
-// (RRA_TREE_G), K = G + 1 FIFO slots per up link (RRA_TREE_K), the
-// broadcast L iterations behind the reduction (RRA_TREE_LAG), stages as
-// shared memory allows; T balanced over whole iterations of one part as in
-// the staged ring.
+// (RRA_TREE_G; at most 24, 12 for bfloat16), K = G + 1 FIFO slots per up
+// link (RRA_TREE_K), the broadcast L = 6 iterations behind the reduction
+// (RRA_TREE_LAG), stages as shared memory allows; T balanced over whole
+// iterations of one part as in the staged ring.  The limits are the best of
+// a sweep on GB300 at 8 ranks x 100 MB (fp32: T 2048, G 12-24, L 6 within
+// 1%; bfloat16: T 1280, G 12, L 6 0.663 ms against 0.700 for T 1024, G 24,
+// L 4).
 rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* out, int n, size_t count,
                              rra_dtype_t dt, cudaStream_t st, int* grid_out) {
   StagedTreeArgs a{};
@@ -452,10 +458,11 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   {
     const size_t ch_est = std::max<size_t>(1, (size_t)s->sms / n);
     const size_t fill = (part + ch_est * 128 - 1) / (ch_est * 128);
-    a.G = (int)std::max(1L, env_long("RRA_TREE_G", (long)std::max<size_t>(1, std::min<size_t>(24, fill))));
+    const size_t gmax = aw == 2 ? 12 : 24;
+    a.G = (int)std::max(1L, env_long("RRA_TREE_G", (long)std::max<size_t>(1, std::min(gmax, fill))));
   }
-  a.lag = (int)std::max(1L, std::min(64L, env_long("RRA_TREE_LAG", aw == 2 ? 4 : 6)));
-  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_TREE_TILE", aw == 2 ? 1024 : 2048)));
+  a.lag = (int)std::max(1L, std::min(64L, env_long("RRA_TREE_LAG", 6)));
+  const long tmax = std::max(64L, std::min(4096L, env_long("RRA_TREE_TILE", aw == 2 ? 1280 : 2048)));
   auto stages_for = [&](long t) {
     const long d = (long)(staged_smem_budget() / ((size_t)t * 16 * (1 + 2 * aw)));
     return (int)std::max(1L, std::min<long>({8L, d, env_long("RRA_TREE_STAGES", 8)}));

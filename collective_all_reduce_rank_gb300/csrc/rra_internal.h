@@ -160,12 +160,21 @@ struct LLArgs {
 constexpr int kDirectThreads = 512;
 constexpr int kRingThreads = 512;
 constexpr int kRingUnitsPerThread = 2;
-// Two-shot: 16-byte units per thread per tile; fewer ranks mean fewer loads
-// per unit, so more units keep the same bytes in flight.
+// Two-shot: 16-byte units per thread per tile, and the CTAs per SM its
+// kernel is compiled for.  Up to four ranks the kernel is built for two
+// CTAs per SM (64 registers a thread): a lane's loads are few there, and
+// twice the warps hide more of the load latency than more units per lane
+// would (on GB300, 2 ranks x 64-256 MiB fp32: one CTA per SM with 4 units a
+// lane reaches 0.60-0.63 of the HBM copy rate); from five ranks a lane's
+// n loads per unit need the registers of one CTA per SM.
 #ifdef __CUDACC__
 __host__ __device__
 #endif
-constexpr int twoshot_units_per_thread(int n) { return n >= 5 ? 1 : (n >= 3 ? 2 : 4); }
+constexpr int twoshot_units_per_thread(int n) { return n >= 3 ? 1 : 2; }
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int twoshot_min_blocks(int n) { return n <= 4 ? 2 : 1; }
 constexpr int kLLThreads = 256;
 
 // SM budget set by rra_set_max_ctas (0: none); kernels_direct.cu caps its

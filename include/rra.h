@@ -73,10 +73,11 @@
  *   RRA_STAGED_SMEM_KB   shared memory for the staged ring's and tree's
  *                        stages (224)
  *   RRA_TREE_TILE, RRA_TREE_G, RRA_TREE_K, RRA_TREE_LAG, RRA_TREE_STAGES,
- *   RRA_TREE_CHANNELS    staged tree: units per message (<= 2048, 1024 for
- *                        bfloat16), tiles per iteration (24), FIFO slots
- *                        (G + 1), iterations the broadcast trails the
- *                        reduction (6, 4 for bfloat16), stages, CTAs per rank
+ *   RRA_TREE_CHANNELS    staged tree: units per message (<= 2048, 1280 for
+ *                        bfloat16), tiles per iteration (by size, at most
+ *                        24, 12 for bfloat16), FIFO slots (G + 1),
+ *                        iterations the broadcast trails the reduction (6),
+ *                        stages, CTAs per rank
  *   RRA_TWOSHOT_CLUSTER  1: two-shot on thread-block clusters
  *   RRA_TWOSHOT_CHANNELS CTAs per rank of two-shot
  *   RRA_TWOSHOT_LAG      tiles the two-shot's gather trails its reduce by
