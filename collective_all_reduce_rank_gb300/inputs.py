@@ -114,3 +114,21 @@ def cfg_sweep(n: int, bytes_per_rank: int, dtype: str, seed: int = 0):
     count = bytes_per_rank // ELEM_SIZE[dtype]
     dist = "int20" if dtype == "int32" else "normal"
     return make_ranks(n, count, dtype, dist, seed, 1.0)
+
+
+def counter_ints(rank: int, idx):
+    """Counter-based integers in [-128, 128) for the element indices ``idx``
+    (an int64 numpy array or torch tensor) of rank ``rank``: a buffer too
+    large to draw and copy from the host is filled on the device with the
+    same values the host computes for a sample of its indices.
+
+    v = ((lo * 0x9E3779B1 + hi * 0x85EBCA77 + (rank + 1) * 0xC2B2AE3D) >> 15)
+        mod 256 - 128, with lo = idx mod 2^20 and hi = idx >> 20: every term
+    stays below 2^53 for idx < 2^34, so int64 arithmetic is exact on both
+    sides, and indices 2^k apart (k >= 20) get unrelated values.  The values
+    are exact in int32, float32 and bfloat16, and so is a sum of up to eight
+    of them in int32 and float32."""
+    lo = idx & 0xFFFFF
+    hi = idx >> 20
+    h = lo * 0x9E3779B1 + hi * 0x85EBCA77 + (rank + 1) * 0xC2B2AE3D
+    return ((h >> 15) & 0xFF) - 128
