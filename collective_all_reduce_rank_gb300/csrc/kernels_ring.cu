@@ -63,10 +63,16 @@ struct RingWarp {
   int r, prev, next, lane;
   uint64_t E;
   uint32_t tag;
-  uint64_t *head_in, *tail_in, *head_out, *tail_out;
-  char *fifo_in, *fifo_out;
+  uint32_t lin, lout;  // counter index of the incoming and outgoing link (and warp)
   uint32_t m_in = 0, m_out = 0;
   uint64_t seen_head = 0, seen_tail = 0;  // last values observed by the polling lanes
+  // Per-message state kept incrementally, so that no step divides by a
+  // runtime value (a warp alone on its SM pays the full latency of every
+  // dependent instruction, and a division is a chain of dozens): the slot
+  // of the next message each way and its index, its LL flag, and the
+  // message count modulo G.
+  char *sin, *sout;
+  uint32_t kin = 0, kout = 0, fin, fout, gin = 0, gout = 0;
 
   __device__ RingWarp(const RingArgs& args, int r_, int ch, int warp, int lane_, int W, uint64_t E_,
                       uint32_t tag_)
@@ -76,36 +82,46 @@ struct RingWarp {
     next = (r + 1) % n;
     const size_t link_in = (size_t)prev * a.channels + ch;
     const size_t link_out = (size_t)r * a.channels + ch;
-    head_in = a.head + link_in * W + warp;
-    tail_in = a.tail + link_in * W + warp;
-    head_out = a.head + link_out * W + warp;
-    tail_out = a.tail + link_out * W + warp;
+    lin = (uint32_t)(link_in * W + warp);
+    lout = (uint32_t)(link_out * W + warp);
     const size_t wregion = (size_t)warp * 32 * UPT * AW * WB;
-    fifo_in = a.fifo + link_in * a.K * a.slot_bytes + wregion;
-    fifo_out = a.fifo + link_out * a.K * a.slot_bytes + wregion;
+    sin = a.fifo + link_in * a.K * a.slot_bytes + wregion;
+    sout = a.fifo + link_out * a.K * a.slot_bytes + wregion;
+    fin = fout = ((tag & 0x7FFFFu) | 0x80000u) << 12;
   }
 
-  // Flag of message m: the slot's round m / K (12 bits) under the call tag
-  // (19 bits, top bit always set, so never 0).  A slot can hold lines of
+  // LL flag of a message: the slot's round m / K (12 bits) under the call
+  // tag (19 bits, top bit always set, so never 0).  A slot can hold lines of
   // any older round -- the messages between may have been empty and never
   // written -- so the round itself must match, not just its parity; the
-  // host keeps a call under 4096 rounds per slot.
-  __device__ __forceinline__ uint32_t ll_flag(uint32_t m) const {
-    return ((((tag & 0x7FFFFu) | 0x80000u)) << 12) | ((m / (uint32_t)a.K) & 0xFFFu);
-  }
+  // host keeps a call under 4096 rounds per slot.  fin / fout hold the flag
+  // of the next message in / out; the round advances when the slot index
+  // wraps.
+  __device__ __forceinline__ static uint32_t next_round(uint32_t f) { return (f & ~0xFFFu) | ((f + 1u) & 0xFFFu); }
 
   // Wait for the next incoming message (Simple: lane 0 acquires the head
   // counter) and / or a free outgoing slot (lane 1 acquires the tail
   // counter); the two waits run side by side.  False: the call aborted.
   __device__ __forceinline__ bool wait(bool need_in, bool need_out, int step) {
     int ok = 1;
+    // (the out-of-line wait writes the value it saw through a pointer: a
+    // copy, so that no pointer into this object escapes and its state stays
+    // in registers)
     if (PROTO == kProtoSimple && need_in && lane == 0) {
       const uint64_t want = E | (uint64_t)(m_in + 1);
-      if (seen_head < want) ok = wait_geq(head_in, want, &seen_head, a.wait, tag, r, prev, step);
+      if (seen_head < want) {
+        uint64_t seen = seen_head;
+        ok = wait_geq(a.head + lin, want, &seen, a.wait, tag, r, prev, step);
+        seen_head = seen;
+      }
     }
     if (need_out && lane == 1 && m_out >= (uint32_t)a.K) {
       const uint64_t want = E | (uint64_t)(m_out - a.K + 1);
-      if (seen_tail < want) ok = wait_geq(tail_out, want, &seen_tail, a.wait, tag, r, next, step);
+      if (seen_tail < want) {
+        uint64_t seen = seen_tail;
+        ok = wait_geq(a.tail + lout, want, &seen, a.wait, tag, r, next, step);
+        seen_tail = seen;
+      }
     }
     ok = __all_sync(0xffffffffu, ok);
     __syncwarp();
@@ -118,29 +134,42 @@ struct RingWarp {
     if (PROTO == kProtoSimple) {
       if (lane == 0) {
         fence_acq_rel();
-        if (sent) st_relaxed(head_out, E | (uint64_t)(m_out + 1));
-        if (consumed) st_relaxed(tail_in, E | (uint64_t)(m_in + 1));
+        if (sent) st_relaxed(a.head + lout, E | (uint64_t)(m_out + 1));
+        if (consumed) st_relaxed(a.tail + lin, E | (uint64_t)(m_in + 1));
       }
     } else if (lane == 0) {
       // a credit is a release (the slot's lines were read before it); a
       // call too short to reuse any slot needs none, which takes the
       // release off every hop of a small message
-      if (consumed && !a.no_credits && ((m_in + 1) % (uint32_t)a.G) == 0)
-        st_release(tail_in, E | (uint64_t)(m_in + 1));
+      if (consumed && !a.no_credits && gin + 1 == (uint32_t)a.G) st_release(a.tail + lin, E | (uint64_t)(m_in + 1));
       // progress marker only (the lines carry their own flags): lets a peer
       // that gives up tell a rank that never sent from one stuck behind it
-      if (sent && ((m_out + 1) % (uint32_t)a.G) == 0) st_relaxed(head_out, E | (uint64_t)(m_out + 1));
+      if (sent && gout + 1 == (uint32_t)a.G) st_relaxed(a.head + lout, E | (uint64_t)(m_out + 1));
     }
-    if (sent) ++m_out;
-    if (consumed) ++m_in;
+    if (sent) {
+      ++m_out;
+      if (++gout == (uint32_t)a.G) gout = 0;
+      sout += a.slot_bytes;
+      if (++kout == (uint32_t)a.K) {
+        kout = 0;
+        sout -= (size_t)a.K * a.slot_bytes;
+        fout = next_round(fout);
+      }
+    }
+    if (consumed) {
+      ++m_in;
+      if (++gin == (uint32_t)a.G) gin = 0;
+      sin += a.slot_bytes;
+      if (++kin == (uint32_t)a.K) {
+        kin = 0;
+        sin -= (size_t)a.K * a.slot_bytes;
+        fin = next_round(fin);
+      }
+    }
   }
 
-  __device__ __forceinline__ char* slot_in() const {
-    return fifo_in + (size_t)(m_in % (uint32_t)a.K) * a.slot_bytes;
-  }
-  __device__ __forceinline__ char* slot_out() const {
-    return fifo_out + (size_t)(m_out % (uint32_t)a.K) * a.slot_bytes;
-  }
+  __device__ __forceinline__ char* slot_in() const { return sin; }
+  __device__ __forceinline__ char* slot_out() const { return sout; }
 
   // unit j of this lane, word q, in a slot
   __device__ __forceinline__ size_t word_off(int j, int q) const {
@@ -152,9 +181,8 @@ struct RingWarp {
     if (PROTO == kProtoSimple) {
       st_l2(p, w);
     } else {
-      const uint32_t f = ll_flag(m_out);
-      st_ll_pair(p, f, w.x, w.y);
-      st_ll_pair(p + 16, f, w.z, w.w);
+      st_ll_pair(p, fout, w.x, w.y);
+      st_ll_pair(p + 16, fout, w.z, w.w);
     }
   }
 
@@ -169,7 +197,7 @@ struct RingWarp {
           if (q < nw && v[j] > 0) w[j][q] = ld_l2(slot + word_off(j, q));
       return true;
     }
-    const uint32_t f = ll_flag(m_in);
+    const uint32_t f = fin;
     bool done = false;
     uint64_t t0 = 0;
     int ok = 1;
@@ -198,7 +226,7 @@ struct RingWarp {
         if (aborted(a.wait.status, tag)) {
           give_up = 1;
         } else if (globaltimer() - t0 > a.wait.timeout_ns || it >= kMaxSpin) {
-          const bool root = (ld_acquire(head_in) >> 32) != (E >> 32);  // prev sent nothing
+          const bool root = (ld_acquire(a.head + lin) >> 32) != (E >> 32);  // prev sent nothing
           record_error(a.wait.status, RRA_ERR_TIMEOUT, r, prev, step, tag, root);
           give_up = 1;
         }
@@ -229,21 +257,36 @@ struct RingWarp {
   // each; in all-gather mode only the own shard.
   uint4 xn[UPT];
   int vn[UPT];
-  uint64_t xq = 0, xq_total = 0;
-  int ch_ = 0;
-  size_t wofs_ = 0;
+  uint32_t xq = 0, xq_total = 0;  // below 2^31, as the message counters
+  // where message xq reads the own input: read xk of its iteration (the
+  // reduce-scatter's chunk r-xk-1, or chunk r), slice xg, first unit xbase
+  int xk = 0, xg = 0;
+  size_t xbase = 0;
 
   __device__ __forceinline__ void prefetch_x() {
     if (xq >= xq_total) return;
-    const int n = a.n, G = a.G;
-    const int XK = a.mode == kRingAllGather ? 1 : n;
-    const uint64_t per = (uint64_t)XK * G;
-    const size_t it = (size_t)(xq / per);
-    const int rem = (int)(xq % per);
-    const int k = rem / G, g = rem % G;
-    const int c = a.mode == kRingAllGather ? r : (k <= n - 2 ? ((r - k - 1) % n + n) % n : r);
-    const size_t base = (it * a.channels + ch_) * (size_t)G * a.slice_units + wofs_ + (size_t)g * a.slice_units;
-    load_x(c, base, xn, vn);
+    int c = r;
+    if (a.mode != kRingAllGather && xk <= a.n - 2) {
+      c = r - xk - 1;
+      if (c < 0) c += a.n;
+    }
+    load_x(c, xbase, xn, vn);
+  }
+
+  // the next such message: slice g + 1, else the next read, else the next
+  // iteration (C x G slices further on)
+  __device__ __forceinline__ void advance_x() {
+    ++xq;
+    const size_t slice = (size_t)a.slice_units;
+    xbase += slice;
+    if (++xg == a.G) {
+      xg = 0;
+      xbase -= (size_t)a.G * slice;
+      if (++xk == (a.mode == kRingAllGather ? 1 : a.n)) {
+        xk = 0;
+        xbase += (size_t)a.channels * a.G * slice;
+      }
+    }
   }
 
   __device__ __forceinline__ void take_x(uint4* xv, int* v) {
@@ -252,7 +295,7 @@ struct RingWarp {
       xv[j] = xn[j];
       v[j] = vn[j];
     }
-    ++xq;
+    advance_x();
     prefetch_x();
   }
 
@@ -355,7 +398,7 @@ struct RingWarp {
     return true;
   }
 
-  __device__ void run(int ch, int warp) {
+  __device__ __forceinline__ void run(int ch, int warp) {
     const int n = a.n, C = a.channels, G = a.G;
     const size_t slice = (size_t)a.slice_units;
     size_t maxu = 0;
@@ -366,16 +409,15 @@ struct RingWarp {
     const size_t per_iter = (size_t)C * G * slice;
     const size_t iters = (maxu + per_iter - 1) / per_iter;
     const size_t wofs = (size_t)warp * 32 * UPT;
-    ch_ = ch;
-    wofs_ = wofs;
-    xq_total = (uint64_t)iters * (a.mode == kRingAllGather ? 1 : n) * G;
+    xbase = (size_t)ch * G * slice + wofs;
+    xq_total = (uint32_t)(iters * (a.mode == kRingAllGather ? 1 : n) * G);
     prefetch_x();
     for (size_t it = 0; it < iters; ++it) {
       const size_t it_base = (it * C + ch) * G * slice + wofs;
       int step = 0;
       if (a.mode != kRingAllGather) {
         for (int s = 0; s + 1 < n; ++s, ++step) {
-          const int c = ((r - s - 1) % n + n) % n;
+          const int c = r - s - 1 < 0 ? r - s - 1 + n : r - s - 1;
           for (int g = 0; g < G; ++g)
             if (!rs_step(c, s == 0, it_base + (size_t)g * slice, step)) return;
         }
@@ -391,7 +433,7 @@ struct RingWarp {
       }
       // all-gather steps 1 .. n-1: receive chunk (r - s) mod n
       for (int s = 1; s < n; ++s, ++step) {
-        const int c = ((r - s) % n + n) % n;
+        const int c = r - s < 0 ? r - s + n : r - s;
         const bool last = s == n - 1;
         for (int g = 0; g < G; ++g)
           if (!ag_step(c, last, it_base + (size_t)g * slice, step)) return;
