@@ -314,19 +314,22 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
 // The ring's form, by measured size ([AIH] "Protocols": LL for small
 // messages, Simple for large ones).  RRA_RING_PROTO=ll | simple | staged
 // forces one.  On 16-byte aligned buffers the staged form (Simple links,
-// whole-CTA messages) is the fastest for large chunks and at 2 ranks (where
-// its first message needs no hop); the per-warp LL form for small and
-// mid-size chunks at 4 ranks and more, where both are bound by the ring's
-// 2(n-1) hops and an LL hop is the cheaper (CUDA graph of 50 calls): fp32 at
-// 8 ranks 28 against 39 us at 1-4 KiB per rank, 34.5 against 40.6 at
-// 32 KiB, 40.0 against 44.3 at 1 MiB, 44.7 against 46.5 at 2 MiB, then
-// slower (95 against 51 at 4 MiB); at 4 ranks 14.7 against 18.6 at 1-2 KiB,
-// 17.5 against 19.4 at 16-32 KiB, a tie from 64 KiB to 1 MiB; bf16, whose
-// LL lines carry fp32 partials, to 32 KiB per rank at 8 ranks and 2 KiB at 4.
-// So LL takes chunks up to 256 KiB (bf16 4 KiB) at n >= 8 and up to 8 KiB
-// (bf16 512 B) at 4 <= n < 8; RRA_RING_LL_STAGED_MAX_BYTES overrides the
-// limit.  Without 16-byte alignment the per-warp LL form takes chunks up to
-// RRA_RING_LL_MAX_BYTES (64 KiB) and the per-warp Simple form larger ones.
+// whole-CTA messages) is the fastest for large chunks; the per-warp LL form
+// for small and mid-size ones, where both are bound by the ring's 2(n-1)
+// hops and an LL hop is the cheaper.  Measured on GB300 (CUDA graph of 50
+// calls, microseconds per call, LL against staged): fp32 at 8 ranks 17.7
+// against 36.2 at 1 KiB per rank, 27.5 against 44.3 at 1 MiB, 29.5 against
+// 46.8 at 2 MiB, then 59.2 against 50.8 at 4 MiB; at 4 ranks 9.5 against
+// 16.8 at 1 KiB, 15.2 against 20.8 at 1 MiB, 24.4 against 21.7 at 2 MiB; at
+// 2 ranks 5.3 against 6.7 at 1 KiB, 7.8 against 8.4 at 128 KiB, a tie at
+// 256-512 KiB, 12.6 against 8.9 at 1 MiB.  bf16, whose LL lines carry fp32
+// partials: at 4 and 8 ranks LL ahead up to 8 KiB chunks (13.0 against 16.3
+// at 4 x 4 KiB, 33.3 against 41.1 at 8 x 64 KiB), behind from 16 KiB; at 2
+// ranks only at 1 KiB per rank.  So LL takes chunks up to 256 KiB (bf16
+// 8 KiB) at n >= 3 and up to 128 KiB (bf16 512 B) at n = 2;
+// RRA_RING_LL_STAGED_MAX_BYTES overrides the limit.  Without 16-byte
+// alignment the per-warp LL form takes chunks up to RRA_RING_LL_MAX_BYTES
+// (64 KiB) and the per-warp Simple form larger ones.
 enum RingForm { kFormWarpSimple = 0, kFormWarpLL = 1, kFormStaged = 2 };
 
 int ring_form(size_t chunk_bytes, bool staged_ok, int n, rra_dtype_t dt) {
@@ -337,8 +340,8 @@ int ring_form(size_t chunk_bytes, bool staged_ok, int n, rra_dtype_t dt) {
   if (staged_ok) {
     static const long ll_max = env_long("RRA_RING_LL_STAGED_MAX_BYTES", -1);
     const long lim = ll_max >= 0 ? ll_max
-                     : dt == RRA_BFLOAT16 ? (n >= 8 ? 4096L : 512L) : (n >= 8 ? 256L << 10 : 8192L);
-    return (n >= 4 && (long)chunk_bytes <= lim) ? kFormWarpLL : kFormStaged;
+                     : dt == RRA_BFLOAT16 ? (n >= 3 ? 8192L : 512L) : (n >= 3 ? 256L << 10 : 128L << 10);
+    return (n >= 2 && (long)chunk_bytes <= lim) ? kFormWarpLL : kFormStaged;
   }
   static const long limit = env_long("RRA_RING_LL_MAX_BYTES", 64L << 10);
   return (long)chunk_bytes <= limit ? kFormWarpLL : kFormWarpSimple;

@@ -57,11 +57,11 @@
  *                        every CUDA error to stderr
  *   RRA_RING_PROTO       ring links for every buffer: staged, simple or ll
  *                        (per-warp forms); default by size (below)
- *   RRA_RING_LL_STAGED_MAX_BYTES  on 16-byte aligned buffers with 4 ranks
+ *   RRA_RING_LL_STAGED_MAX_BYTES  on 16-byte aligned buffers with 2 ranks
  *                        or more, chunks up to this many bytes take LL
- *                        lines (measured faster there; default 256 KiB at 8
- *                        ranks and 8 KiB below, bfloat16 4 KiB and 512 B),
- *                        larger ones the staged form
+ *                        lines (measured faster there; default 256 KiB from
+ *                        3 ranks and 128 KiB at 2, bfloat16 8 KiB and
+ *                        512 B), larger ones the staged form
  *   RRA_RING_LL_MAX_BYTES  on other buffers, the largest chunk the per-warp
  *                        ring sends as LL lines (64 KiB; larger: Simple)
  *   RRA_RING_CLUSTER     1: the ring on thread-block clusters
