@@ -72,6 +72,7 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
   };
   if (iters > 0) load_x(0);
   uint64_t seen = 0;  // polling lane j's last observed value of peer (r + j)'s flag
+  size_t due = F;     // reduced tiles after which the next progress flag goes up
 
   for (size_t it = 0; it < iters + F; ++it) {
     // 1. gather loads of tile gi = it - F
@@ -130,11 +131,14 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
           if (vy[j][i - 1] > 0) store_out<DT, VEC, true>(dst, u0 + 32 * j, vy[j][i - 1], y[j][i - 1]);
       }
     }
-    // 5. progress: tiles 0..it reduced
-    if (reduce && ((it + 1) % F == 0 || it + 1 == iters)) {
+    // 5. progress: tiles 0..it reduced (every F tiles and after the last)
+    if (reduce && (it + 1 == due || it + 1 == iters)) {
       __syncwarp();
       if (lane == 0) st_release(my_flag, E | (uint64_t)(it + 1));
+      due += F;
     }
+    // trips after the last reduce and before the first gather do nothing
+    if (it + 1 >= iters && it + 1 < F) it = F - 1;
   }
 }
 
