@@ -840,12 +840,14 @@ def tp_latency(torch, rra, inputs, stream, reps=100):
 # the ring's link forms against size (the protocol crossover)
 # --------------------------------------------------------------------------
 def run_ring_forms(args):
-    """The ring all-reduce per size in its default form (the one the
-    library picks by size) and forced into the staged form (Simple links)
-    and the per-warp LL form: n = 2, 4, 8, fp32 and bf16, 1 KiB .. 16 MiB per
-    rank, a CUDA graph of 50 calls per point (hot L2).  The forms must agree
-    bit for bit (the same ring order); a point where they do not, or where a
-    wait expired, stops the run."""
+    """The ring and the tree all-reduce per size in their default form (the
+    one the library picks by size) and forced into the staged form (Simple
+    links, whole-CTA messages by bulk copies) and the per-warp LL form: n =
+    2, 4, 8, fp32 and bf16, 1 KiB .. 16 MiB per rank, a CUDA graph of 50
+    calls per point (hot L2).  The forms of a schedule must agree bit for
+    bit (the same order); a point where they do not, or where a wait
+    expired, stops the run.  An LL tree whose lines do not fit the
+    workspace's LL region has no time (null)."""
     import torch
 
     import collective_all_reduce_rank_gb300 as rra
@@ -855,38 +857,48 @@ def run_ring_forms(args):
     rra.rra_init(0)
     stream = torch.cuda.Stream()
     out = open(args.ring_forms, "w")
-    for dtype, code in (("float32", rra.RRA_FLOAT32), ("bfloat16", rra.RRA_BFLOAT16)):
-        for n in inputs.SWEEP_RANKS:
-            for k in range(10, 25):
-                S = 1 << k
-                xs = inputs.cfg_sweep(n, S, dtype, seed=S + n)
-                count = xs[0].size
-                if dtype == "bfloat16":
-                    ins = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
-                else:
-                    ins = [torch.from_numpy(x).cuda() for x in xs]
-                outs = [torch.empty_like(x) for x in ins]
-                call = lambda: rra.rra_allreduce(ins, outs, count, code, rra.RRA_SUM, rra.RRA_ALGO_RING, stream)
-                row = {"dtype": dtype, "n": n, "bytes_per_rank": S}
-                row["default_us"], _, _ = time_call(torch, call, stream, 0)
-                ref = [o.clone() for o in outs]
-                for form in ("staged", "ll"):
-                    os.environ["RRA_RING_PROTO"] = form
-                    try:
-                        row[form + "_us"], _, _ = time_call(torch, call, stream, 0)
-                    finally:
-                        os.environ.pop("RRA_RING_PROTO")
-                    if not all(torch.equal(a, b) for a, b in zip(ref, outs)):
-                        raise SystemExit("ring forms disagree at n=%d %s %d (%s)" % (n, dtype, S, form))
-                st, info = rra.rra_query_status(stream)
-                if st != 0:
-                    raise SystemExit("device status %d %s" % (st, info))
-                for key in ("default_us", "staged_us", "ll_us"):
-                    row[key] = round(row[key], 2)
-                row["fastest"] = min(("staged", "ll"), key=lambda f: row[f + "_us"])
-                out.write(json.dumps(row) + "\n")
-                out.flush()
-                print(json.dumps(row), flush=True)
+    for algo, code_algo, env in (("ring", rra.RRA_ALGO_RING, "RRA_RING_PROTO"),
+                                 ("tree", rra.RRA_ALGO_TREE, "RRA_TREE_PROTO")):
+        for dtype, code in (("float32", rra.RRA_FLOAT32), ("bfloat16", rra.RRA_BFLOAT16)):
+            for n in inputs.SWEEP_RANKS:
+                for k in range(10, 25):
+                    S = 1 << k
+                    xs = inputs.cfg_sweep(n, S, dtype, seed=S + n)
+                    count = xs[0].size
+                    if dtype == "bfloat16":
+                        ins = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
+                    else:
+                        ins = [torch.from_numpy(x).cuda() for x in xs]
+                    outs = [torch.empty_like(x) for x in ins]
+                    call = lambda: rra.rra_allreduce(ins, outs, count, code, rra.RRA_SUM, code_algo, stream)
+                    row = {"algo": algo, "dtype": dtype, "n": n, "bytes_per_rank": S}
+                    row["default_us"], _, _ = time_call(torch, call, stream, 0)
+                    ref = [o.clone() for o in outs]
+                    for form in ("staged", "ll"):
+                        os.environ[env] = form
+                        try:
+                            st = rra.rra_allreduce(ins, outs, count, code, rra.RRA_SUM, code_algo, stream,
+                                                   check=False)
+                            if st == rra.RRA_ERR_WORKSPACE:
+                                row[form + "_us"] = None
+                                continue
+                            row[form + "_us"], _, _ = time_call(torch, call, stream, 0)
+                        finally:
+                            os.environ.pop(env)
+                        if not all(torch.equal(a, b) for a, b in zip(ref, outs)):
+                            raise SystemExit("%s forms disagree at n=%d %s %d (%s)" % (algo, n, dtype, S, form))
+                    st, info = rra.rra_query_status(stream)
+                    if st != 0:
+                        raise SystemExit("device status %d %s" % (st, info))
+                    for key in ("default_us", "staged_us", "ll_us"):
+                        if row[key] is not None:
+                            row[key] = round(row[key], 2)
+                    timed = [f for f in ("staged", "ll") if row[f + "_us"] is not None]
+                    row["fastest"] = min(timed, key=lambda f: row[f + "_us"])
+                    out.write(json.dumps(row) + "\n")
+                    out.flush()
+                    print(json.dumps(row), flush=True)
+                    del ins, outs, ref
     out.close()
 
 
@@ -1199,7 +1211,7 @@ def main():
     ap.add_argument("--no-next", action="store_true", help="skip the rows beyond the step (tree, RMSNorm, ...)")
     ap.add_argument("--no-small", action="store_true", help="skip the TP-activation latency table")
     ap.add_argument("--ring-forms", default=None,
-                    help="write the ring's default, staged and LL forms against size to this JSONL file")
+                    help="write the ring and tree default, staged and LL forms against size to this JSONL file")
     ap.add_argument("--ll-sweep", default=None,
                     help="write the LL / LL128 payload sweep (1 KiB .. 256 MiB, 4 sources) to this JSONL file")
     ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")

@@ -70,6 +70,19 @@ __device__ __forceinline__ void st_volatile8(void* p, uint32_t a, uint32_t b) {
   asm volatile("st.volatile.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
 }
 
+// Two LL lines (8 bytes each: a 4-byte data word under a 4-byte flag) in
+// one 16-byte access; each 8-byte line is single-copy atomic, so a reader
+// that sees a line's flag sees its data.
+__device__ __forceinline__ void st_ll_pair(void* p, uint32_t flag, uint32_t a, uint32_t b) {
+  const unsigned long long x = ((unsigned long long)flag << 32) | a;
+  const unsigned long long y = ((unsigned long long)flag << 32) | b;
+  asm volatile("st.volatile.global.v2.u64 [%0], {%1,%2};" ::"l"(p), "l"(x), "l"(y) : "memory");
+}
+
+__device__ __forceinline__ void ld_ll_pair(const void* p, unsigned long long& x, unsigned long long& y) {
+  asm volatile("ld.volatile.global.v2.u64 {%0,%1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+}
+
 __device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
   uint64_t v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");

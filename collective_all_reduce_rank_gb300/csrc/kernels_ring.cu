@@ -40,16 +40,6 @@
 
 namespace rra {
 
-__device__ __forceinline__ void st_ll_pair(void* p, uint32_t flag, uint32_t a, uint32_t b) {
-  const unsigned long long x = ((unsigned long long)flag << 32) | a;
-  const unsigned long long y = ((unsigned long long)flag << 32) | b;
-  asm volatile("st.volatile.global.v2.u64 [%0], {%1,%2};" ::"l"(p), "l"(x), "l"(y) : "memory");
-}
-
-__device__ __forceinline__ void ld_ll_pair(const void* p, unsigned long long& x, unsigned long long& y) {
-  asm volatile("ld.volatile.global.v2.u64 {%0,%1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
-}
-
 template <int DT, bool VEC, int PROTO>
 struct RingWarp {
   static constexpr int PU = Elem<DT>::kPerUnit;

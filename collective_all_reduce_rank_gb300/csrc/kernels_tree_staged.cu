@@ -56,6 +56,7 @@
 // Needs 16-byte aligned buffers.  The last tile's partial 16-byte unit is
 // read and written element-wise by the consumers.
 #include "staged.cuh"
+#include "tree.cuh"
 
 namespace rra {
 
@@ -66,36 +67,6 @@ constexpr int kTreeFirstConsumer = kTreeSignaller + 1;
 constexpr int kTreeThreads = (kTreeFirstConsumer + kTreeConsumers) * 32;
 constexpr int kTreeMaxStages = 8;
 constexpr int kTreeNT = kTreeConsumers * 32;
-
-// rank at heap position `pos` of tree t
-__device__ __forceinline__ int tree_rank_at(int t, int n, int pos) { return t == 0 ? pos : n - 1 - pos; }
-
-// Rank r's place in tree t.
-struct TreeRole {
-  int parent;      // the parent's rank (the root: its own)
-  int kid[2];      // the children's ranks, position 2p+1 first (-1: none)
-  int nk;          // children
-  bool root;       // position 0
-  bool leaf;       // below the root, no children: sends nothing up
-  bool lc[2];      // child i is a leaf: its partial is its input
-};
-
-__device__ __forceinline__ TreeRole tree_role(int t, int n, int r) {
-  const int p = t == 0 ? r : n - 1 - r;
-  TreeRole o;
-  o.root = p == 0;
-  o.parent = o.root ? r : tree_rank_at(t, n, (p - 1) / 2);
-  o.nk = 0;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int c = 2 * p + 1 + i;
-    o.kid[i] = c < n ? tree_rank_at(t, n, c) : -1;
-    o.lc[i] = c < n && 2 * c + 1 >= n;
-    o.nk += c < n ? 1 : 0;
-  }
-  o.leaf = !o.root && o.nk == 0;
-  return o;
-}
 
 // The CTA's message classes: 0 = up messages of tree 0, 1 = up messages of
 // tree 1, 2 = down messages of tree 0, 3 = down messages of tree 1; class
@@ -142,26 +113,6 @@ struct TreeShared {
   uint32_t abort;
   uint32_t epoch;
 };
-
-// a += w, w in accumulator words (a partial sum from a child)
-template <int DT>
-__device__ __forceinline__ void acc_add_words(Acc& a, const uint4* w) {
-  if constexpr (DT == RRA_INT32) {
-    a.w[0] += w[0].x;
-    a.w[1] += w[0].y;
-    a.w[2] += w[0].z;
-    a.w[3] += w[0].w;
-  } else {
-    constexpr int AW = Elem<DT>::kAccWords;
-#pragma unroll
-    for (int q = 0; q < AW; ++q) {
-      const uint32_t v[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        a.w[4 * q + i] = __float_as_uint(__fadd_rn(__uint_as_float(a.w[4 * q + i]), __uint_as_float(v[i])));
-    }
-  }
-}
 
 template <int DT>
 __global__ void __launch_bounds__(kTreeThreads, 1) tree_staged_kernel(const __grid_constant__ StagedTreeArgs a) {

@@ -506,6 +506,76 @@ rra_status_t run_tree_staged(DevState* s, const void* const* in, void* const* ou
   return cuda_status(launch_tree_staged(dt, a, n * (int)c, st));
 }
 
+// LL double tree (small messages): warp tiles of 32 x kTreeLLUnits units,
+// one per warp while the SMs hold enough CTAs of 8 warps (more tiles loop);
+// both line regions of every rank (up: units x AW x 32 bytes, down: units x
+// 32) must fit the workspace's LL region.
+rra_status_t run_tree_ll(DevState* s, const void* const* in, void* const* out, int n, size_t count,
+                         rra_dtype_t dt, cudaStream_t st, int* grid_out) {
+  TreeLLArgs a{};
+  const size_t e = elem_size(dt), aw = dt == RRA_BFLOAT16 ? 2 : 1, pu = 16 / e;
+  for (int r = 0; r < n; ++r) {
+    a.in[r] = in[r];
+    a.out[r] = out[r];
+  }
+  a.n = n;
+  a.count = count;
+  const size_t units = (count * e + 15) / 16;
+  // chunk plan for two parts, as the staged tree
+  const size_t h = std::min(count, ((count + 1) / 2 + pu - 1) / pu * pu);
+  a.half_units = (h + pu - 1) / pu;
+  a.up_bytes = units * aw * 32;
+  a.dn_bytes = units * 32;
+  if ((size_t)n * (a.up_bytes + a.dn_bytes) > s->ws.ll_bytes) return RRA_ERR_WORKSPACE;
+  const size_t part = std::max(a.half_units, units - a.half_units);
+  const size_t tu = 32 * (size_t)kTreeLLUnits, warps = kTreeLLThreads / 32;
+  const size_t tiles = (part + tu - 1) / tu;
+  int occ = 0;
+  cudaError_t err = tree_ll_occupancy(dt, &occ);
+  if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
+  long c = std::min<long>({(long)std::max<size_t>(1, (tiles + warps - 1) / warps), (long)(s->sms * occ / n),
+                           channel_cap(n), env_long("RRA_TREE_CHANNELS", kMaxChannels)});
+  if (c < 1) return RRA_ERR_UNSUPPORTED;
+  a.channels = (int)c;
+  a.lines = s->ws.ll;
+  a.joined = s->ws.flags + 2 * kLinkFlags;  // the two-shot progress words, unused by a tree call
+  a.wait = wait_cfg(s);
+  *grid_out = n * (int)c;
+  return cuda_status(launch_tree_ll(dt, a, n * (int)c, st));
+}
+
+// The tree's form: RRA_TREE_PROTO=ll | staged forces one; by default LL
+// lines for messages up to tree_ll_max_bytes per rank whose lines fit the
+// LL region, the staged tree above.  Measured on GB300 (CUDA graph of 50
+// calls, microseconds per call, LL against staged): fp32 at 8 ranks 6.3
+// against 18.6 at 1 KiB per rank, 11.5 against 26.6 at 256 KiB, 13.5
+// against 30.7 at 512 KiB; at 2 ranks 4.0 against 7.0 at 1 KiB, 9.9
+// against 13.4 at 2 MiB; bf16 at 8 ranks 6.9 against 18.9 at 1 KiB, 19.7
+// against 31.0 at 512 KiB; at 2 ranks 7.7 against 11.2 at 1 MiB and 13.9
+// against 13.6 at 2 MiB.  LL is ahead wherever its lines fit the 32 MiB
+// region of the default workspace (1 MiB per rank at 4 ranks, 512 KiB at
+// 8), but for bf16 at 2 MiB per rank.
+size_t tree_ll_max_bytes(int n, rra_dtype_t dt);
+
+rra_status_t run_tree(DevState* s, const void* const* in, void* const* out, int n, size_t count, rra_dtype_t dt,
+                      cudaStream_t st, int* grid_out) {
+  const char* p = std::getenv("RRA_TREE_PROTO");
+  if (p && !std::strcmp(p, "ll")) return run_tree_ll(s, in, out, n, count, dt, st, grid_out);
+  if (p && !std::strcmp(p, "staged")) return run_tree_staged(s, in, out, n, count, dt, st, grid_out);
+  const size_t e = elem_size(dt), aw = dt == RRA_BFLOAT16 ? 2 : 1;
+  const size_t units = (count * e + 15) / 16;
+  if (count * e <= tree_ll_max_bytes(n, dt) && (size_t)n * units * 32 * (aw + 1) <= s->ws.ll_bytes)
+    return run_tree_ll(s, in, out, n, count, dt, st, grid_out);
+  return run_tree_staged(s, in, out, n, count, dt, st, grid_out);
+}
+
+size_t tree_ll_max_bytes(int n, rra_dtype_t dt) {
+  static const long lim = env_long("RRA_TREE_LL_MAX_BYTES", -1);
+  if (lim >= 0) return (size_t)lim;
+  (void)n;
+  return dt == RRA_BFLOAT16 ? (1u << 20) : (2u << 20);
+}
+
 // mode: kRingAllReduce / kRingReduceScatter / kRingAllGather.  ibase, obase,
 // len: per chunk, in elements.
 rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int n, int mode,
@@ -591,7 +661,8 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   cudaError_t err = ring_occupancy(dt, vec, proto, &occ);
   if (err != cudaSuccess || occ < 1) return cuda_status(err == cudaSuccess ? cudaErrorInvalidConfiguration : err);
   const size_t need = (maxu + (size_t)a.G * a.slice_units - 1) / ((size_t)a.G * a.slice_units);
-  const size_t fifo_cap = s->ws.fifo_bytes / ((size_t)n * a.K * a.slot_bytes);
+  // LL lines live in their own region (never a raw word under a poll)
+  const size_t fifo_cap = (proto == kProtoLL ? s->ws.ll_bytes : s->ws.fifo_bytes) / ((size_t)n * a.K * a.slot_bytes);
   long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
                            (long)fifo_cap, env_long("RRA_RING_CHANNELS", 16), channel_cap(n)});
   if (fifo_cap < 1) return RRA_ERR_WORKSPACE;
@@ -620,7 +691,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
     }
   }
   a.channels = (int)c;
-  a.fifo = s->ws.fifo;
+  a.fifo = proto == kProtoLL ? s->ws.ll : s->ws.fifo;
   a.head = s->ws.flags;
   a.tail = s->ws.flags + kLinkFlags;
   a.wait = wait_cfg(s);
@@ -739,7 +810,10 @@ rra_status_t rra_init(int device, size_t workspace_bytes) {
   s.ws.sync = reinterpret_cast<SyncHdr*>(p + 64);
   s.ws.flags = reinterpret_cast<uint64_t*>(p + kFlagOffset);
   s.ws.fifo = p + kFifoOffset;
-  s.ws.fifo_bytes = bytes > kFifoOffset ? bytes - kFifoOffset : 0;
+  const size_t slots = bytes > kFifoOffset ? (bytes - kFifoOffset) / 256 * 256 : 0;
+  s.ws.ll_bytes = slots / 4 / 256 * 256;
+  s.ws.fifo_bytes = slots - s.ws.ll_bytes;
+  s.ws.ll = s.ws.fifo + s.ws.fifo_bytes;
   s.ready = true;
   load_default_tuning();
   return RRA_SUCCESS;
@@ -939,7 +1013,7 @@ rra_status_t rra_allreduce(const void* const* bufs, void* const* outs, int nrank
   int grid = 0;
   rra_status_t rs;
   if (algo == RRA_ALGO_TREE) {
-    rs = run_tree_staged(s, bufs, outs, nranks, count, dtype, st, &grid);
+    rs = run_tree(s, bufs, outs, nranks, count, dtype, st, &grid);
   } else if (algo == RRA_ALGO_TWO_SHOT) {
     rs = run_twoshot(s, bufs, outs, nranks, count, dtype, vec, st, &grid);
   } else {

@@ -21,7 +21,12 @@ constexpr int kMaxChannels = 80;  // CTAs per virtual rank in persistent kernels
 //   [64, 128)      SyncHdr: call epoch + end-of-kernel arrival counter
 //   [256, ...)     step flags, one uint64 per (link or rank, channel, warp):
 //                  ring head, ring tail, two-shot progress
-//   [kFifoOffset, end) ring FIFO slots
+//   [kFifoOffset, +fifo_bytes) FIFO slots of raw data (the staged ring and
+//                  tree, the per-warp Simple ring)
+//   [ll, end)      LL lines (the per-warp LL ring, the LL tree), a quarter
+//                  of the slot space: a region that only ever holds LL
+//                  lines, so that a poll never meets a raw data word that
+//                  happens to equal its flag
 // ---------------------------------------------------------------------------
 // A wait that expires records where: bit 63 set, bits 32..62 index (step
 // or line), bits 16..31 the rank waited for (0xFFFF: none), bits 0..15 the
@@ -56,6 +61,8 @@ struct Workspace {
   uint64_t* flags;  // kFlagWords entries
   char* fifo;
   size_t fifo_bytes;
+  char* ll;
+  size_t ll_bytes;
 };
 
 // Settings every waiting kernel gets by value.
@@ -139,6 +146,26 @@ struct StagedTreeArgs {
   int K;            // FIFO slots per link
   int stages;       // shared-memory stages per CTA
   int lag;          // iterations the broadcast trails the reduction by (>= 1)
+  WaitCfg wait;
+};
+
+// LL double binary tree all-reduce for small messages (persistent,
+// cooperative): every node posts its partial as LL lines in its up region,
+// every node with children its totals in its down region; each line is
+// written once per call, so no slot is reused and no credit is needed.
+// Rank r's regions: up at lines + r * (up_bytes + dn_bytes) (unit u's
+// accumulator words at u * AW * 32), down right after (unit u at u * 32).
+struct TreeLLArgs {
+  const void* in[kMaxRanks];
+  void* out[kMaxRanks];
+  size_t count;       // elements per rank
+  size_t half_units;  // 16-byte units of the part reduced on tree 0 (the rest: tree 1)
+  char* lines;
+  size_t up_bytes;    // per rank: units x AW x 32
+  size_t dn_bytes;    // per rank: units x 32
+  uint64_t* joined;   // [n x channels]: the call's epoch once the CTA has started
+  int n;
+  int channels;
   WaitCfg wait;
 };
 
@@ -236,6 +263,13 @@ cudaError_t launch_ring_cluster(int dt, const RingArgs& a, int grid, cudaStream_
 size_t ring_staged_smem(int dt, int tile_units, int stages);
 cudaError_t ring_staged_occupancy(int dt, int tile_units, int stages, int* max_blocks_per_sm);
 cudaError_t launch_ring_staged(int dt, const RingArgs& a, int grid, cudaStream_t s);
+
+// LL tree: 16-byte aligned buffers; kTreeLLThreads threads, each lane
+// kTreeLLUnits units per tile.
+constexpr int kTreeLLThreads = 256;
+constexpr int kTreeLLUnits = 2;
+cudaError_t tree_ll_occupancy(int dt, int* max_blocks_per_sm);
+cudaError_t launch_tree_ll(int dt, const TreeLLArgs& a, int grid, cudaStream_t s);
 
 // Staged tree: 16-byte aligned buffers.
 size_t tree_staged_smem(int dt, int tile_units, int stages);

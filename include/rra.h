@@ -78,6 +78,10 @@
  *                        24, 12 for bfloat16), FIFO slots (G + 1),
  *                        iterations the broadcast trails the reduction (6),
  *                        stages, CTAs per rank
+ *   RRA_TREE_PROTO       ll | staged: the tree's form (default: LL lines up
+ *                        to RRA_TREE_LL_MAX_BYTES per rank, 2 MiB, bfloat16
+ *                        1 MiB, where its lines fit a quarter of the
+ *                        workspace's slot space; the staged tree above)
  *   RRA_TWOSHOT_CLUSTER  1: two-shot on thread-block clusters
  *   RRA_TWOSHOT_CHANNELS CTAs per rank of two-shot
  *   RRA_TWOSHOT_LAG      tiles the two-shot's gather trails its reduce by
@@ -145,7 +149,9 @@ typedef enum {
    *  sums its own data, then the partial of its child 2p+1, then that of
    *  its child 2p+2; each root's total, rounded once, travels down
    *  unchanged.  Needs 16-byte aligned buffers (else
-   *  RRA_ERR_UNSUPPORTED).  Links through the workspace. */
+   *  RRA_ERR_UNSUPPORTED).  Links through the workspace: LL lines for
+   *  small messages ("Protocols": LL for small messages), whole-CTA
+   *  messages staged by bulk copies for large ones. */
   RRA_ALGO_TREE = 6
 } rra_algo_t;
 
@@ -154,8 +160,9 @@ typedef enum {
 /* ------------------------------------------------------------------------ */
 
 /** Create the per-device state: the workspace (device status word, step
- *  flags, ring FIFO slots) of `workspace_bytes` bytes (0 = 128 MiB, at least
- *  1 MiB) on CUDA device `device`, which becomes current.  Fixed buffers
+ *  flags, FIFO slots; a quarter of the slot space holds LL lines only) of
+ *  `workspace_bytes` bytes (0 = 128 MiB, at least 1 MiB) on CUDA device
+ *  `device`, which becomes current.  Fixed buffers
  *  made once, ahead of the calls, keep every call allocation-free and
  *  graph-capturable, as [AIH] "Exercises" 3 explains for custom
  *  all-reduce.  Calling it again for an initialised device is a no-op that

@@ -24,14 +24,14 @@ def _init():
 
 @pytest.mark.parametrize("algo,proto", [(rra.RRA_ALGO_RING, "simple"), (rra.RRA_ALGO_RING, "ll"),
                                         (rra.RRA_ALGO_RING, "staged"), (rra.RRA_ALGO_TWO_SHOT, None),
-                                        (rra.RRA_ALGO_TREE, None)])
+                                        (rra.RRA_ALGO_TREE, "staged"), (rra.RRA_ALGO_TREE, "ll")])
 @pytest.mark.parametrize("skip", [0, 3])
 def test_crashed_rank_times_out_and_gpu_stays_usable(algo, proto, skip, monkeypatch):
     import gpu_util as g
 
     if proto:
-        monkeypatch.setenv("RRA_RING_PROTO", proto)
-    n, count = 4, 1 << 20
+        monkeypatch.setenv("RRA_TREE_PROTO" if algo == rra.RRA_ALGO_TREE else "RRA_RING_PROTO", proto)
+    n, count = 4, 1 << 16 if proto == "ll" and algo == rra.RRA_ALGO_TREE else 1 << 20
     xs = inputs.make_ranks(n, count, "float32", "normal", seed=1)
     ins = [g.to_dev(x, "float32") for x in xs]
     outs = g.empty(n, count, "float32")

@@ -51,7 +51,8 @@ def test_staged_tree_shapes(tile, G, K, stages, dtype, n, count, monkeypatch):
     # the oracle's tree bits, twice in a row and in place
     import gpu_util as g
 
-    for k, v in (("RRA_TREE_TILE", tile), ("RRA_TREE_G", G), ("RRA_TREE_K", K), ("RRA_TREE_STAGES", stages)):
+    for k, v in (("RRA_TREE_TILE", tile), ("RRA_TREE_G", G), ("RRA_TREE_K", K), ("RRA_TREE_STAGES", stages),
+                 ("RRA_TREE_PROTO", "staged")):
         monkeypatch.setenv(k, str(v))
     dist = "int20" if dtype == "int32" else "normal"
     xs = inputs.make_ranks(n, count, dtype, dist, seed=count + n + tile)
@@ -76,7 +77,7 @@ def test_staged_tree_lag(lag, tile, G, K, stages, dtype, n, count, monkeypatch):
     import gpu_util as g
 
     for k, v in (("RRA_TREE_TILE", tile), ("RRA_TREE_G", G), ("RRA_TREE_K", K), ("RRA_TREE_STAGES", stages),
-                 ("RRA_TREE_LAG", lag)):
+                 ("RRA_TREE_LAG", lag), ("RRA_TREE_PROTO", "staged")):
         monkeypatch.setenv(k, str(v))
     xs = inputs.make_ranks(n, count, dtype, "normal", seed=count + n + lag)
     want, _, _ = oracle.allreduce("tree", xs, dtype)
@@ -89,13 +90,15 @@ def test_staged_tree_lag(lag, tile, G, K, stages, dtype, n, count, monkeypatch):
         g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "staged tree lag=%d n=%d r=%d" % (lag, n, r))
 
 
-def test_tree_order_case_on_gpu():
+@pytest.mark.parametrize("form", ["staged", "ll"])
+def test_tree_order_case_on_gpu(form, monkeypatch):
     # the hand-derived n = 4 double-tree case of the oracle's pins, x =
     # (0.5, 2^25, 2, -2^25) on every element of each rank: 2.5 on the part
     # tree 0 sums, (x0 + (x1 + x3)) + x2, and 2 on tree 1's part,
-    # (x3 + (x2 + x0)) + x1; many tiles in each part
+    # (x3 + (x2 + x0)) + x1; many tiles in each part, in both forms
     import gpu_util as g
 
+    monkeypatch.setenv("RRA_TREE_PROTO", form)
     B = float(2 ** 25)
     count = 4 * 40_000
     xs = [np.full(count, v, np.float32) for v in (0.5, B, 2.0, -B)]
@@ -116,3 +119,48 @@ def test_tree_rejects_unaligned():
     outs = g.empty(2, 1001, "float32")
     st = rra.rra_allreduce(ins, outs, 1001, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE, check=False)
     assert st == rra.RRA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16", "int32"])
+@pytest.mark.parametrize("n,count", [(2, 1), (2, 400_003), (3, 7), (4, 4096), (5, 100_003), (7, 65_537),
+                                     (8, 5), (8, 20_480), (8, 240_007)])
+def test_ll_tree_matches_oracle(dtype, n, count, monkeypatch):
+    # the LL form forced over shapes: one unit, ragged tails, one tile per
+    # warp and several (8 x 240,007 fp32 and 2 x 400,003 loop their warps),
+    # in place and out of place, twice in a row (every line carries the
+    # call's tag, so the first call's lines never satisfy the second's polls)
+    import gpu_util as g
+
+    monkeypatch.setenv("RRA_TREE_PROTO", "ll")
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, count, dtype, dist, seed=count + n + 17)
+    want, _, _ = oracle.allreduce("tree", xs, dtype)
+    for inplace in (False, True):
+        for rep in range(2):
+            ins = [g.to_dev(x, dtype) for x in xs]
+            outs = ins if inplace else g.empty(n, count, dtype)
+            rra.rra_allreduce(ins, outs, count, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_TREE)
+            st, info = rra.rra_query_status()
+            assert st == 0, info
+            for r in range(n):
+                got = g.to_host(outs[r], dtype)
+                if dtype == "bfloat16":
+                    assert g.bf16_rel_ok(got, want[r])
+                g.assert_bits_equal(got, want[r], "LL tree n=%d r=%d inplace=%s rep=%d" % (n, r, inplace, rep))
+
+
+def test_ll_tree_too_large_for_its_region(monkeypatch):
+    # forced LL on a message whose lines do not fit the LL region: a
+    # workspace error, no launch
+    import gpu_util as g
+
+    monkeypatch.setenv("RRA_TREE_PROTO", "ll")
+    n, count = 8, 1 << 22
+    ins = [g.to_dev(np.ones(count, np.float32), "float32") for _ in range(n)]
+    outs = g.empty(n, count, "float32")
+    st = rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE, check=False)
+    assert st == rra.RRA_ERR_WORKSPACE
+    monkeypatch.setenv("RRA_TREE_PROTO", "staged")
+    rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE)
+    assert rra.rra_query_status()[0] == 0
+    assert np.all(g.to_host(outs[3], "float32") == 8.0)
