@@ -24,7 +24,7 @@ using namespace rra;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kDefaultWorkspace = 128ull << 20;
+constexpr size_t kDefaultWorkspace = 256ull << 20;
 constexpr uint64_t kDefaultTimeoutNs = 500ull * 1000 * 1000;
 
 struct DevState {
@@ -325,8 +325,8 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
 // 256-512 KiB, 12.6 against 8.9 at 1 MiB.  bf16, whose LL lines carry fp32
 // partials: at 4 and 8 ranks LL ahead up to 8 KiB chunks (13.0 against 16.3
 // at 4 x 4 KiB, 33.3 against 41.1 at 8 x 64 KiB), behind from 16 KiB; at 2
-// ranks only at 1 KiB per rank.  So LL takes chunks up to 256 KiB (bf16
-// 8 KiB) at n >= 3 and up to 128 KiB (bf16 512 B) at n = 2;
+// ranks up to 4 KiB per rank.  So LL takes chunks up to 256 KiB (bf16
+// 8 KiB) at n >= 3 and up to 128 KiB (bf16 2 KiB) at n = 2;
 // RRA_RING_LL_STAGED_MAX_BYTES overrides the limit.  Without 16-byte
 // alignment the per-warp LL form takes chunks up to RRA_RING_LL_MAX_BYTES
 // (64 KiB) and the per-warp Simple form larger ones.
@@ -340,7 +340,7 @@ int ring_form(size_t chunk_bytes, bool staged_ok, int n, rra_dtype_t dt) {
   if (staged_ok) {
     static const long ll_max = env_long("RRA_RING_LL_STAGED_MAX_BYTES", -1);
     const long lim = ll_max >= 0 ? ll_max
-                     : dt == RRA_BFLOAT16 ? (n >= 3 ? 8192L : 512L) : (n >= 3 ? 256L << 10 : 128L << 10);
+                     : dt == RRA_BFLOAT16 ? (n >= 3 ? 8192L : 2048L) : (n >= 3 ? 256L << 10 : 128L << 10);
     return (n >= 2 && (long)chunk_bytes <= lim) ? kFormWarpLL : kFormStaged;
   }
   static const long limit = env_long("RRA_RING_LL_MAX_BYTES", 64L << 10);
@@ -552,9 +552,10 @@ rra_status_t run_tree_ll(DevState* s, const void* const* in, void* const* out, i
 // against 30.7 at 512 KiB; at 2 ranks 4.0 against 7.0 at 1 KiB, 9.9
 // against 13.4 at 2 MiB; bf16 at 8 ranks 6.9 against 18.9 at 1 KiB, 19.7
 // against 31.0 at 512 KiB; at 2 ranks 7.7 against 11.2 at 1 MiB and 13.9
-// against 13.6 at 2 MiB.  LL is ahead wherever its lines fit the 32 MiB
-// region of the default workspace (1 MiB per rank at 4 ranks, 512 KiB at
-// 8), but for bf16 at 2 MiB per rank.
+// against 13.6 at 2 MiB; with a 64 MiB region fp32 at 2 ranks x 4 MiB
+// 17.7 against 21.2 and bf16 at 4 ranks x 2 MiB 23.7 against 29.0.  LL is
+// ahead wherever its lines fit, but for bf16 at 2 ranks above 1 MiB per
+// rank; up to 4 MiB per rank it is taken when they fit.
 size_t tree_ll_max_bytes(int n, rra_dtype_t dt);
 
 rra_status_t run_tree(DevState* s, const void* const* in, void* const* out, int n, size_t count, rra_dtype_t dt,
@@ -572,8 +573,7 @@ rra_status_t run_tree(DevState* s, const void* const* in, void* const* out, int 
 size_t tree_ll_max_bytes(int n, rra_dtype_t dt) {
   static const long lim = env_long("RRA_TREE_LL_MAX_BYTES", -1);
   if (lim >= 0) return (size_t)lim;
-  (void)n;
-  return dt == RRA_BFLOAT16 ? (1u << 20) : (2u << 20);
+  return dt == RRA_BFLOAT16 && n == 2 ? (1u << 20) : (4u << 20);
 }
 
 // mode: kRingAllReduce / kRingReduceScatter / kRingAllGather.  ibase, obase,
@@ -811,7 +811,10 @@ rra_status_t rra_init(int device, size_t workspace_bytes) {
   s.ws.flags = reinterpret_cast<uint64_t*>(p + kFlagOffset);
   s.ws.fifo = p + kFifoOffset;
   const size_t slots = bytes > kFifoOffset ? (bytes - kFifoOffset) / 256 * 256 : 0;
-  s.ws.ll_bytes = slots / 4 / 256 * 256;
+  // LL lines: 64 MiB (the per-warp LL ring's 16 channels x 16 slots of
+  // 32 KiB per link at 8 ranks x 256 KiB chunks; the LL tree's lines up to
+  // 1 MiB per rank at 8 ranks), at most half the slot space
+  s.ws.ll_bytes = std::min<size_t>(64ull << 20, slots / 2 / 256 * 256);
   s.ws.fifo_bytes = slots - s.ws.ll_bytes;
   s.ws.ll = s.ws.fifo + s.ws.fifo_bytes;
   s.ready = true;

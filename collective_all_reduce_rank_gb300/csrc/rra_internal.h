@@ -23,8 +23,8 @@ constexpr int kMaxChannels = 80;  // CTAs per virtual rank in persistent kernels
 //                  ring head, ring tail, two-shot progress
 //   [kFifoOffset, +fifo_bytes) FIFO slots of raw data (the staged ring and
 //                  tree, the per-warp Simple ring)
-//   [ll, end)      LL lines (the per-warp LL ring, the LL tree), a quarter
-//                  of the slot space: a region that only ever holds LL
+//   [ll, end)      LL lines (the per-warp LL ring, the LL tree), 64 MiB,
+//                  at most half the slots: a region that only ever holds LL
 //                  lines, so that a poll never meets a raw data word that
 //                  happens to equal its flag
 // ---------------------------------------------------------------------------

@@ -61,7 +61,7 @@
  *                        or more, chunks up to this many bytes take LL
  *                        lines (measured faster there; default 256 KiB from
  *                        3 ranks and 128 KiB at 2, bfloat16 8 KiB and
- *                        512 B), larger ones the staged form
+ *                        2 KiB), larger ones the staged form
  *   RRA_RING_LL_MAX_BYTES  on other buffers, the largest chunk the per-warp
  *                        ring sends as LL lines (64 KiB; larger: Simple)
  *   RRA_RING_CLUSTER     1: the ring on thread-block clusters
@@ -79,9 +79,9 @@
  *                        iterations the broadcast trails the reduction (6),
  *                        stages, CTAs per rank
  *   RRA_TREE_PROTO       ll | staged: the tree's form (default: LL lines up
- *                        to RRA_TREE_LL_MAX_BYTES per rank, 2 MiB, bfloat16
- *                        1 MiB, where its lines fit a quarter of the
- *                        workspace's slot space; the staged tree above)
+ *                        to RRA_TREE_LL_MAX_BYTES per rank, 4 MiB, bfloat16
+ *                        at 2 ranks 1 MiB, where its lines fit the
+ *                        workspace's LL region; the staged tree above)
  *   RRA_TWOSHOT_CLUSTER  1: two-shot on thread-block clusters
  *   RRA_TWOSHOT_CHANNELS CTAs per rank of two-shot
  *   RRA_TWOSHOT_LAG      tiles the two-shot's gather trails its reduce by
@@ -160,8 +160,8 @@ typedef enum {
 /* ------------------------------------------------------------------------ */
 
 /** Create the per-device state: the workspace (device status word, step
- *  flags, FIFO slots; a quarter of the slot space holds LL lines only) of
- *  `workspace_bytes` bytes (0 = 128 MiB, at least 1 MiB) on CUDA device
+ *  flags, FIFO slots; 64 MiB of them, at most half, hold LL lines only) of
+ *  `workspace_bytes` bytes (0 = 256 MiB, at least 1 MiB) on CUDA device
  *  `device`, which becomes current.  Fixed buffers
  *  made once, ahead of the calls, keep every call allocation-free and
  *  graph-capturable, as [AIH] "Exercises" 3 explains for custom
