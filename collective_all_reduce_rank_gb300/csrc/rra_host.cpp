@@ -552,10 +552,11 @@ rra_status_t run_tree_ll(DevState* s, const void* const* in, void* const* out, i
 // against 30.7 at 512 KiB; at 2 ranks 4.0 against 7.0 at 1 KiB, 9.9
 // against 13.4 at 2 MiB; bf16 at 8 ranks 6.9 against 18.9 at 1 KiB, 19.7
 // against 31.0 at 512 KiB; at 2 ranks 7.7 against 11.2 at 1 MiB and 13.9
-// against 13.6 at 2 MiB; with a 64 MiB region fp32 at 2 ranks x 4 MiB
-// 17.7 against 21.2 and bf16 at 4 ranks x 2 MiB 23.7 against 29.0.  LL is
-// ahead wherever its lines fit, but for bf16 at 2 ranks above 1 MiB per
-// rank; up to 4 MiB per rank it is taken when they fit.
+// against 13.6 at 2 MiB; with the 64 MiB region, up to the largest
+// messages whose lines fit, fp32 at 2 ranks x 8 MiB 27.4 against 32.7, at
+// 4 x 4 MiB 30.3 against 48.2, at 8 x 2 MiB 27.4 against 56.1, bf16 at 4
+// ranks x 2 MiB 23.1 against 29.5.  So LL wherever its lines fit, but for
+// bf16 at 2 ranks above 1 MiB per rank.
 size_t tree_ll_max_bytes(int n, rra_dtype_t dt);
 
 rra_status_t run_tree(DevState* s, const void* const* in, void* const* out, int n, size_t count, rra_dtype_t dt,
@@ -573,7 +574,7 @@ rra_status_t run_tree(DevState* s, const void* const* in, void* const* out, int 
 size_t tree_ll_max_bytes(int n, rra_dtype_t dt) {
   static const long lim = env_long("RRA_TREE_LL_MAX_BYTES", -1);
   if (lim >= 0) return (size_t)lim;
-  return dt == RRA_BFLOAT16 && n == 2 ? (1u << 20) : (4u << 20);
+  return dt == RRA_BFLOAT16 && n == 2 ? (size_t)1 << 20 : SIZE_MAX;
 }
 
 // mode: kRingAllReduce / kRingReduceScatter / kRingAllGather.  ibase, obase,

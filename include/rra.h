@@ -78,10 +78,10 @@
  *                        24, 12 for bfloat16), FIFO slots (G + 1),
  *                        iterations the broadcast trails the reduction (6),
  *                        stages, CTAs per rank
- *   RRA_TREE_PROTO       ll | staged: the tree's form (default: LL lines up
- *                        to RRA_TREE_LL_MAX_BYTES per rank, 4 MiB, bfloat16
- *                        at 2 ranks 1 MiB, where its lines fit the
- *                        workspace's LL region; the staged tree above)
+ *   RRA_TREE_PROTO       ll | staged: the tree's form (default: LL lines
+ *                        wherever they fit the workspace's LL region, up to
+ *                        RRA_TREE_LL_MAX_BYTES per rank (no limit; bfloat16
+ *                        at 2 ranks 1 MiB); the staged tree otherwise)
  *   RRA_TWOSHOT_CLUSTER  1: two-shot on thread-block clusters
  *   RRA_TWOSHOT_CHANNELS CTAs per rank of two-shot
  *   RRA_TWOSHOT_LAG      tiles the two-shot's gather trails its reduce by

@@ -166,26 +166,29 @@ def test_fitted_alpha_beta_prior(lib, tmp_path):
 
 def test_shipped_tuning_table(lib):
     # the table made by the size sweep on a GB300 loads, covers n = 2, 4, 8
-    # for int32, bfloat16 and float32 from 1 KiB to 1 GiB, and says one-shot
-    # at every point (on one GPU it moves the floor bytes with one
-    # synchronization); the fitted prior picks one-shot for rank counts the
-    # table lacks
+    # for int32, bfloat16 and float32 from 1 KiB to 1 GiB, and the selector
+    # returns its pick at every point; below 64 MiB per rank, where a call
+    # is bound by its synchronizations, the pick is one-shot (one sync); the
+    # fitted prior picks one-shot for rank counts the table lacks
     path = os.path.join(os.path.dirname(rra.__file__), "tune", "gb300.txt")
     lines = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
     rows = [r for r in lines if r[0] != "ab"]
     prior = [r for r in lines if r[0] == "ab"]
     types = ("int32", "bfloat16", "float32")
+    code = {"ring": rra.RRA_ALGO_RING, "one_shot": rra.RRA_ALGO_ONE_SHOT, "two_shot": rra.RRA_ALGO_TWO_SHOT,
+            "tree": rra.RRA_ALGO_TREE}
+    dcode = {"int32": rra.RRA_INT32, "bfloat16": rra.RRA_BFLOAT16, "float32": rra.RRA_FLOAT32}
     assert {(int(r[0]), r[1]) for r in rows} == {(n, d) for n in (2, 4, 8) for d in types}
     assert {int(r[2]) for r in rows} == set(range(10, 31))
+    assert {r[3] for r in rows} <= set(code)
     # the fitted prior covers every type and schedule
     assert {(r[1], r[2]) for r in prior} == {(d, a) for d in types for a in ("ring", "one_shot", "two_shot", "tree")}
     assert rra.rra_load_tuning(path) == rra.RRA_SUCCESS
     try:
-        assert {r[3] for r in rows} == {"one_shot"}
-        for n in (2, 4, 8):
-            for size in (1 << 10, 1 << 20, 1 << 26):
-                assert rra.rra_select_algo(n, size, rra.RRA_BFLOAT16) == rra.RRA_ALGO_ONE_SHOT
-                assert rra.rra_select_algo(n, size, rra.RRA_FLOAT32) == rra.RRA_ALGO_ONE_SHOT
+        for n, dt, lb, algo in rows:
+            assert rra.rra_select_algo(int(n), 1 << int(lb), dcode[dt]) == code[algo], (n, dt, lb)
+            if int(lb) < 26:
+                assert algo == "one_shot", (n, dt, lb)
         for n in (3, 5, 6, 7):
             for size in (1 << 10, 1 << 30):
                 assert rra.rra_select_algo(n, size, rra.RRA_FLOAT32) == rra.RRA_ALGO_ONE_SHOT
