@@ -29,9 +29,11 @@
 //   LL: every 4-byte word travels in an 8-byte line with a flag, written
 //     and read as one 64-bit access (single-copy atomic), so no fence and
 //     no head counter are needed: the receiver polls the lines themselves.
-//     The flag is the call tag doubled plus the slot's reuse parity, so a
-//     line left from the slot's previous use or an earlier call never
-//     matches.  Credits are raised once per G messages.
+//     The flag carries the call tag (19 bits, bit 31 set) and the slot's
+//     round (12 bits), so a line left from the slot's previous use or an
+//     earlier call never matches; the lines live in the workspace's LL
+//     region, which holds nothing but LL lines.  Credits are raised once
+//     per G messages, and not at all in a call too short to reuse a slot.
 // The rank's own input for the next message is loaded before its wait, so
 // the HBM latency overlaps the wait.  bfloat16 partial sums travel as
 // float32 and are rounded once, at the final reduce-scatter step.  Only the
