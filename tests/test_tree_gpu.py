@@ -164,3 +164,27 @@ def test_ll_tree_too_large_for_its_region(monkeypatch):
     rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE)
     assert rra.rra_query_status()[0] == 0
     assert np.all(g.to_host(outs[3], "float32") == 8.0)
+
+
+@pytest.mark.parametrize("max_ctas", [1, 8, 19])
+@pytest.mark.parametrize("form", ["staged", "ll"])
+def test_tree_under_sm_budget(max_ctas, form, monkeypatch):
+    # an SM budget leaves the tree one or a few channels per rank: its warps
+    # (LL) or CTAs (staged) loop over many tiles; the oracle's bits
+    import gpu_util as g
+
+    monkeypatch.setenv("RRA_TREE_PROTO", form)
+    n, count = 8, 100_003
+    xs = inputs.make_ranks(n, count, "float32", "normal", seed=max_ctas + 7)
+    want, _, _ = oracle.allreduce("tree", xs, "float32")
+    ins = [g.to_dev(x, "float32") for x in xs]
+    outs = g.empty(n, count, "float32")
+    rra.rra_set_max_ctas(max_ctas)
+    try:
+        rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TREE)
+        st, info = rra.rra_query_status()
+    finally:
+        rra.rra_set_max_ctas(0)
+    assert st == 0, info
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], "float32"), want[r], "tree %s max_ctas=%d r=%d" % (form, max_ctas, r))
