@@ -666,7 +666,14 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   const size_t fifo_cap = (proto == kProtoLL ? s->ws.ll_bytes : s->ws.fifo_bytes) / ((size_t)n * a.K * a.slot_bytes);
   long c = std::min<long>({(long)kMaxChannels, (long)(s->sms * occ / n), (long)std::max<size_t>(1, need),
                            (long)fifo_cap, env_long("RRA_RING_CHANNELS", 16), channel_cap(n)});
-  if (fifo_cap < 1) return RRA_ERR_WORKSPACE;
+  if (fifo_cap < 1) {
+    // a small workspace's LL region may not hold one channel of LL slots;
+    // the staged form sizes its slots by the message (unless a form was
+    // forced)
+    if (proto == kProtoLL && staged_ok && !std::getenv("RRA_RING_PROTO"))
+      return run_ring_staged(s, a, maxu, dt, st, grid_out);
+    return RRA_ERR_WORKSPACE;
+  }
   if (c < 1) return RRA_ERR_UNSUPPORTED;
   if (proto == kProtoLL) {
     // LL line flags carry the slot round in 12 bits: more rounds than that
