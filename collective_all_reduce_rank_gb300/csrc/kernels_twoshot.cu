@@ -6,10 +6,11 @@
 // reduce-scatter); in the second it reads the sums back (an all-gather);
 // two synchronizations.
 //
-// One persistent cooperative launch of n x C CTAs.  CTA (r, ch) is channel
-// ch of virtual rank r; its 16 warps are independent pipelines, each lane
-// with 2 (two ranks) or 1 16-byte units per tile; up to four ranks two CTAs
-// share an SM.  Warp w handles its part of tile t of
+// One persistent cooperative launch of n x C CTAs, two per SM.  CTA (r, ch)
+// is channel ch of virtual rank r.  Up to four ranks (the fused form) its
+// 16 warps are independent pipelines, each lane with 2 (two ranks) or 1
+// 16-byte units per tile; from five ranks (the split form, below) 8 warps
+// reduce and 8 gather.  In the fused form warp w handles its part of tile t of
 // every chunk in turn and, in trip i of its loop,
 //   1. issues the loads of the all-gather part of tile i - F: the other
 //      ranks' sums, from outs[q] (L2), after acquiring their progress;
@@ -142,6 +143,87 @@ __device__ __forceinline__ void twoshot_warp(const TwoShotArgs& a, int r, int ch
   }
 }
 
+// Split form (five ranks and more): warps 0..W/2-1 reduce, warp W/2 + w
+// gathers what reducer w of every other rank posts.  Reducers never wait;
+// a gatherer waits on the peers' progress flags of its pipeline.
+template <int N, int DT, bool VEC>
+__device__ __forceinline__ void twoshot_split_warp(const TwoShotArgs& a, int r, int ch, int warp, int lane,
+                                                   int W, uint64_t E, uint32_t tag) {
+  constexpr int PU = Elem<DT>::kPerUnit;
+  constexpr int ES = Elem<DT>::kSize;
+  const size_t F = a.lag > 0 ? (size_t)a.lag : (size_t)twoshot_lag<N>();
+  const int WR = W / 2;
+  const bool reducer = warp < WR;
+  const int pw = reducer ? warp : warp - WR;  // pipeline
+  const int C = a.channels;
+  const size_t tile = (size_t)a.tile_units;  // = WR * 32
+  const size_t per_iter = (size_t)C * tile;
+  const size_t iters = ((a.chunk_len[0] + PU - 1) / PU + per_iter - 1) / per_iter;  // chunk 0 is the longest
+  auto first_of = [&](size_t it) { return (it * C + ch) * tile + (size_t)pw * 32; };
+  if (reducer) {
+    uint64_t* my_flag = a.progress + ((size_t)r * C + ch) * W + pw;
+    const size_t lo = a.chunk_lo[r] * ES;
+    const size_t len = a.chunk_len[r];
+    uint4 x[N];
+    int v = 0;
+    auto load_x = [&](size_t it) {
+      const size_t u = first_of(it) + lane;
+      v = unit_valid<DT>(u, len);
+      if (v > 0) {
+#pragma unroll
+        for (int k = 0; k < N; ++k) x[k] = load_in<DT, VEC>(static_cast<const char*>(a.in[k]) + lo, u, v);
+      }
+    };
+    if (iters > 0) load_x(0);
+    size_t due = F;
+    for (size_t it = 0; it < iters; ++it) {
+      if (v > 0) {
+        Acc s;
+        acc_init<DT>(s, x[0]);
+#pragma unroll
+        for (int k = 1; k < N; ++k) acc_add<DT>(s, x[k]);
+        store_out<DT, VEC, false>(static_cast<char*>(a.out[r]) + lo, first_of(it) + lane, v, acc_narrow<DT>(s));
+      }
+      if (it + 1 < iters) load_x(it + 1);
+      if (it + 1 == due || it + 1 == iters) {
+        __syncwarp();
+        if (lane == 0) st_release(my_flag, E | (uint64_t)(it + 1));
+        due += F;
+      }
+    }
+    return;
+  }
+  uint64_t seen = 0;  // polling lane j's last observed value of peer (r + j)'s flag
+  for (size_t gi = 0; gi < iters; ++gi) {
+    int ok = 1;
+    if (lane >= 1 && lane < N) {
+      const int q = (r + lane) % N;
+      const uint64_t want = E | (uint64_t)(gi + 1);
+      if (first_of(gi) < (a.chunk_len[q] + PU - 1) / PU && seen < want)
+        ok = wait_geq(a.progress + ((size_t)q * C + ch) * W + pw, want, &seen, a.wait, tag, r, q, (int)gi);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    __syncwarp();
+    if (!ok) return;
+    const size_t u = first_of(gi) + lane;
+    uint4 y[N - 1];
+    int vy[N - 1];
+#pragma unroll
+    for (int i = 1; i < N; ++i) {
+      const int q = (r + i) % N;
+      const char* src = static_cast<const char*>(a.out[q]) + a.chunk_lo[q] * ES;
+      vy[i - 1] = unit_valid<DT>(u, a.chunk_len[q]);
+      if (vy[i - 1] > 0) y[i - 1] = load_shared_out<DT, VEC>(src, u, vy[i - 1]);
+    }
+#pragma unroll
+    for (int i = 1; i < N; ++i) {
+      const int q = (r + i) % N;
+      char* dst = static_cast<char*>(a.out[r]) + a.chunk_lo[q] * ES;
+      if (vy[i - 1] > 0) store_out<DT, VEC, true>(dst, u, vy[i - 1], y[i - 1]);
+    }
+  }
+}
+
 template <int N, int DT, bool VEC>
 __global__ void __launch_bounds__(kDirectThreads, twoshot_min_blocks(N)) twoshot_kernel(const __grid_constant__ TwoShotArgs a) {
   __shared__ uint32_t s_epoch;
@@ -150,8 +232,12 @@ __global__ void __launch_bounds__(kDirectThreads, twoshot_min_blocks(N)) twoshot
   const uint32_t epoch = s_epoch;
   const int r = blockIdx.x % N, ch = blockIdx.x / N;
   const int W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (r != a.wait.skip_rank)
-    twoshot_warp<N, DT, VEC>(a, r, ch, warp, lane, W, (uint64_t)epoch << 32, epoch + 1u);
+  if (r != a.wait.skip_rank) {
+    if constexpr (twoshot_split(N))
+      twoshot_split_warp<N, DT, VEC>(a, r, ch, warp, lane, W, (uint64_t)epoch << 32, epoch + 1u);
+    else
+      twoshot_warp<N, DT, VEC>(a, r, ch, warp, lane, W, (uint64_t)epoch << 32, epoch + 1u);
+  }
   arrive_end(a.wait.sync, epoch);
 }
 

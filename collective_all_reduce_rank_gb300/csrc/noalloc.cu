@@ -109,7 +109,7 @@ extern "C" rra_status_t rra_allreduce_two_shot_static(const void* const* bufs, v
     a.chunk_len[c] = hi - lo;
     vec = vec && (uintptr_t)bufs[c] % 16 == 0 && (uintptr_t)outs[c] % 16 == 0;
   }
-  a.tile_units = kDirectThreads * twoshot_units_per_thread(nranks);
+  a.tile_units = twoshot_tile_units(nranks);
   int occ = 0, dev = 0, sms = 0;
   if (twoshot_occupancy(nranks, dtype, vec, &occ) != cudaSuccess || occ < 1)
     return record_call(kCall, RRA_ALGO_TWO_SHOT, nranks, count, dtype, 0, RRA_ERR_CUDA);

@@ -290,7 +290,7 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
       return cuda_status(err);
     }
   }
-  a.tile_units = kDirectThreads * twoshot_units_per_thread(n);
+  a.tile_units = twoshot_tile_units(n);
   a.lag = (int)std::max(0L, std::min(256L, env_long("RRA_TWOSHOT_LAG", 0)));
   int occ = 0;
   cudaError_t err = twoshot_occupancy(n, dt, vec, &occ);

@@ -188,12 +188,16 @@ constexpr int kDirectThreads = 512;
 constexpr int kRingThreads = 512;
 constexpr int kRingUnitsPerThread = 2;
 // Two-shot: 16-byte units per thread per tile, and the CTAs per SM its
-// kernel is compiled for.  Up to four ranks the kernel is built for two
-// CTAs per SM (64 registers a thread): a lane's loads are few there, and
-// twice the warps hide more of the load latency than more units per lane
-// would (on GB300, 2 ranks x 64-256 MiB fp32: one CTA per SM with 4 units a
-// lane reaches 0.60-0.63 of the HBM copy rate); from five ranks a lane's
-// n loads per unit need the registers of one CTA per SM.
+// kernel is compiled for: two, so that twice the warps hide the loads'
+// latency (on GB300, 2 ranks x 64-256 MiB fp32: one CTA per SM with 4
+// units a lane reached 0.62-0.64 of the HBM copy rate, two 0.74-0.75).  Up
+// to four ranks every warp reduces and gathers (64 registers a thread: 2
+// units a lane at two ranks, 1 at three and four).  From five ranks a lane
+// holding n inputs and n-1 sums would need the registers of one CTA per
+// SM, so the kernel splits each CTA's warps into reducers (n inputs) and
+// gatherers (n-1 sums), and a tile is then the reducers' units (8 ranks x
+// 64-256 MiB: 0.81-0.82 fused, 0.86-0.90 split; up to four ranks the split
+// measured 2-15% slower than the fused form).
 #ifdef __CUDACC__
 __host__ __device__
 #endif
@@ -201,7 +205,17 @@ constexpr int twoshot_units_per_thread(int n) { return n >= 3 ? 1 : 2; }
 #ifdef __CUDACC__
 __host__ __device__
 #endif
-constexpr int twoshot_min_blocks(int n) { return n <= 4 ? 2 : 1; }
+constexpr int twoshot_min_blocks(int n) { return 2; }
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr bool twoshot_split(int n) { return n >= 5; }
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int twoshot_tile_units(int n) {
+  return twoshot_split(n) ? kDirectThreads / 2 : kDirectThreads * twoshot_units_per_thread(n);
+}
 constexpr int kLLThreads = 256;
 
 // SM budget set by rra_set_max_ctas (0: none); kernels_direct.cu caps its

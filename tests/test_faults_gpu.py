@@ -87,6 +87,33 @@ def test_static_two_shot_silent_rank_times_out_and_recovers(skip):
     assert rra.rra_query_status()[0] == 0
 
 
+@pytest.mark.parametrize("skip", [0, 6])
+def test_split_two_shot_silent_rank_times_out_and_recovers(skip):
+    # the split two-shot (five ranks and more: reducer and gatherer warps):
+    # the gatherers' bounded waits name the silent rank; the next call is
+    # correct
+    import gpu_util as g
+
+    n, count = 8, (1 << 20) + 5
+    xs = inputs.make_ranks(n, count, "float32", "normal", seed=3)
+    ins = [g.to_dev(x, "float32") for x in xs]
+    outs = g.empty(n, count, "float32")
+    rra.rra_set_timeout_ns(1_000_000)  # 1 ms
+    rra.rra_debug_skip_rank(skip)
+    try:
+        rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TWO_SHOT)
+        st, info = rra.rra_query_status()
+    finally:
+        rra.rra_debug_skip_rank(-1)
+        rra.rra_set_timeout_ns(2_000_000_000)
+    assert st == rra.RRA_ERR_TIMEOUT and info[2] == skip, info
+    rra.rra_allreduce(ins, outs, count, rra.RRA_FLOAT32, rra.RRA_SUM, rra.RRA_ALGO_TWO_SHOT)
+    assert rra.rra_query_status()[0] == 0
+    want, _, _ = oracle.allreduce("twoshot", xs, "float32")
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], "float32"), want[r], "split two-shot after recovery")
+
+
 def test_flight_recorder_lists_recent_calls():
     import gpu_util as g
 
