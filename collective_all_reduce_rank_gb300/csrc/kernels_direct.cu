@@ -21,8 +21,19 @@
 
 namespace rra {
 
+// Up to four ranks a thread takes two units per trip (2n loads in flight);
+// from five the kernel is built for two CTAs per SM with one unit per trip
+// (n loads a thread, 53-60 registers at eight ranks against 94): on GB300 at
+// 8 ranks x 8 MiB fp32 0.85 -> 0.90 of the HBM copy rate, bf16 at 64-256
+// MiB 0.88-0.92 -> 0.90-0.93, fp32 at 64-256 MiB within 0.5%.
+template <int N>
+__host__ __device__ constexpr bool oneshot_two_units() {
+  return N <= 4;
+}
+
 template <int N, int DT, bool VEC>
-__global__ void __launch_bounds__(kDirectThreads) oneshot_kernel(const __grid_constant__ DirectArgs a) {
+__global__ void __launch_bounds__(kDirectThreads, oneshot_two_units<N>() ? 1 : 2)
+    oneshot_kernel(const __grid_constant__ DirectArgs a) {
   const size_t count = a.count;
   const size_t units = (count + Elem<DT>::kPerUnit - 1) / Elem<DT>::kPerUnit;
   int r_lo = 0, r_hi = N;
@@ -33,7 +44,7 @@ __global__ void __launch_bounds__(kDirectThreads) oneshot_kernel(const __grid_co
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   // two units per trip: 2N independent 16-byte loads in flight per thread
-  for (; u + stride < units; u += 2 * stride) {
+  for (; oneshot_two_units<N>() && u + stride < units; u += 2 * stride) {
     const size_t u1 = u + stride;
     const int v0 = unit_valid<DT>(u, count), v1 = unit_valid<DT>(u1, count);
     uint4 x0[N], x1[N];
@@ -56,7 +67,7 @@ __global__ void __launch_bounds__(kDirectThreads) oneshot_kernel(const __grid_co
       store_out<DT, VEC, true>(a.out[r], u1, v1, y1);
     }
   }
-  if (u < units) {
+  for (; u < units; u += stride) {
     const int v0 = unit_valid<DT>(u, count);
     uint4 x0[N];
 #pragma unroll
