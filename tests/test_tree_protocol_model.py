@@ -105,11 +105,11 @@ def cursor_sequence(n, r, G, iters, lag):
     return seq
 
 
-def run_model(n, G, K, D, P, iters, seed, lag=1):
+def run_model(n, G, K, D, P, iters, seed, lag=1, cap_loaders=True):
     rnd = random.Random(seed)
     seqs = [tree_messages(n, r, G, iters, lag) for r in range(n)]
     roles = [[role(0, n, r), role(1, n, r)] for r in range(n)]
-    npl = min(P, D)
+    npl = min(P, D) if cap_loaders else P
     info = []
     for r in range(n):
         rows = []
@@ -304,3 +304,16 @@ def test_even_n_every_rank_has_one_heavy_role(n):
         R = [role(0, n, r), role(1, n, r)]
         assert sum(1 for x in R if x["kids"]) == 1
         assert sum(1 for x in R if x["leaf"]) == 1 or any(x["root"] for x in R)
+
+
+def test_uncapped_slot_loaders_alias():
+    # a planted mistake: more P loaders than stages lets some interleaving
+    # pass a stage's parity test a phase early -- the reason the kernel caps
+    # them at the stage count; the model must catch it
+    hits = 0
+    for seed in range(40):
+        try:
+            run_model(4, 2, 3, 1, 3, iters=(3, 3), seed=seed, cap_loaders=False)
+        except Aliasing:
+            hits += 1
+    assert hits > 0
