@@ -47,7 +47,7 @@ struct RingWarp {
   static constexpr int PU = Elem<DT>::kPerUnit;
   static constexpr int ES = Elem<DT>::kSize;
   static constexpr int AW = Elem<DT>::kAccWords;
-  static constexpr int UPT = kRingUnitsPerThread;
+  static constexpr int UPT = ring_units_per_thread(DT, PROTO);
   // bytes a slot reserves per unit (per accumulator word: 16 B Simple, 32 B LL)
   static constexpr int WB = PROTO == kProtoLL ? 32 : 16;
 

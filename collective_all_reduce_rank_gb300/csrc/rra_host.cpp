@@ -317,16 +317,16 @@ rra_status_t run_twoshot(DevState* s, const void* const* in, void* const* out, i
 // whole-CTA messages) is the fastest for large chunks; the per-warp LL form
 // for small and mid-size ones, where both are bound by the ring's 2(n-1)
 // hops and an LL hop is the cheaper.  Measured on GB300 (CUDA graph of 50
-// calls, microseconds per call, LL against staged): fp32 at 8 ranks 17.7
-// against 36.2 at 1 KiB per rank, 27.5 against 44.3 at 1 MiB, 29.5 against
-// 46.8 at 2 MiB, then 59.2 against 50.8 at 4 MiB; at 4 ranks 9.5 against
-// 16.8 at 1 KiB, 15.2 against 20.8 at 1 MiB, 24.4 against 21.7 at 2 MiB; at
-// 2 ranks 5.3 against 6.7 at 1 KiB, 7.8 against 8.4 at 128 KiB, a tie at
-// 256-512 KiB, 12.6 against 8.9 at 1 MiB.  bf16, whose LL lines carry fp32
-// partials: at 4 and 8 ranks LL ahead up to 8 KiB chunks (13.0 against 16.3
-// at 4 x 4 KiB, 33.3 against 41.1 at 8 x 64 KiB), behind from 16 KiB; at 2
-// ranks up to 4 KiB per rank.  So LL takes chunks up to 256 KiB (bf16
-// 8 KiB) at n >= 3 and up to 128 KiB (bf16 2 KiB) at n = 2;
+// calls, microseconds per call, LL against staged): fp32 at 8 ranks 15.6
+// against 36.3 at 1 KiB per rank, 18.2 against 44.3 at 1 MiB, 41.3 against
+// 46.7 at 2 MiB, then 72.3 against 50.7 at 4 MiB; at 4 ranks 8.5 against
+// 16.3 at 1 KiB, 15.6 against 20.8 at 1 MiB, 31.3 against 22.0 at 2 MiB;
+// at 2 ranks 4.9 against 6.4 at 1 KiB, 6.6 against 8.5 at 256 KiB, 8.8
+// against 8.6 at 512 KiB.  bf16, whose LL lines carry fp32 partials: at 8
+// ranks 30.7 against 45.5 at 1 MiB, 57.4 against 48.8 at 2 MiB; at 4 ranks
+// 15.1 against 20.0 at 512 KiB, 23.1 against 21.1 at 1 MiB; at 2 ranks 8.1
+// against 8.4 at 256 KiB, 11.1 against 8.5 at 512 KiB.  So LL takes chunks
+// up to 256 KiB at n >= 3 and 128 KiB at n = 2, bf16 up to 128 KiB;
 // RRA_RING_LL_STAGED_MAX_BYTES overrides the limit.  Without 16-byte
 // alignment the per-warp LL form takes chunks up to RRA_RING_LL_MAX_BYTES
 // (64 KiB) and the per-warp Simple form larger ones.
@@ -340,7 +340,7 @@ int ring_form(size_t chunk_bytes, bool staged_ok, int n, rra_dtype_t dt) {
   if (staged_ok) {
     static const long ll_max = env_long("RRA_RING_LL_STAGED_MAX_BYTES", -1);
     const long lim = ll_max >= 0 ? ll_max
-                     : dt == RRA_BFLOAT16 ? (n >= 3 ? 8192L : 2048L) : (n >= 3 ? 256L << 10 : 128L << 10);
+                     : dt == RRA_BFLOAT16 ? 128L << 10 : (n >= 3 ? 256L << 10 : 128L << 10);
     return (n >= 2 && (long)chunk_bytes <= lim) ? kFormWarpLL : kFormStaged;
   }
   static const long limit = env_long("RRA_RING_LL_MAX_BYTES", 64L << 10);
@@ -642,7 +642,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
   const int form = ring_form(maxu * 16, staged_ok, n, dt);
   if (form == kFormStaged) return run_ring_staged(s, a, maxu, dt, st, grid_out);
   const int proto = form == kFormWarpLL ? kProtoLL : kProtoSimple;
-  a.slice_units = kRingThreads * kRingUnitsPerThread;
+  a.slice_units = kRingThreads * ring_units_per_thread(dt, proto);
   // Credits: a rank's sends minus receives never exceed G.  Simple raises a
   // credit per message, so K > G keeps n full FIFOs from all being pending
   // at once (with K == G every rank could fill its FIFO in the first step
@@ -681,6 +681,7 @@ rra_status_t run_ring(DevState* s, const void* const* in, void* const* out, int 
     const size_t iters = (maxu + (size_t)c * a.G * a.slice_units - 1) / ((size_t)c * a.G * a.slice_units);
     const size_t sends = mode == kRingAllReduce ? 2 * (size_t)(n - 1) : (size_t)(n - 1);
     if (iters * sends * a.G / a.K >= 4096) {
+      a.slice_units = kRingThreads * ring_units_per_thread(dt, kProtoSimple);
       a.K = (int)std::max((long)a.G + 1, env_long("RRA_RING_K", 2L * a.G));
       a.slot_bytes = (size_t)a.slice_units * aw * 16;
       err = ring_occupancy(dt, vec, kProtoSimple, &occ);

@@ -187,6 +187,15 @@ struct LLArgs {
 constexpr int kDirectThreads = 512;
 constexpr int kRingThreads = 512;
 constexpr int kRingUnitsPerThread = 2;
+// per-warp ring: units per lane per message.  LL takes one: a lane then
+// polls 32 bytes of lines a word group (64 for bfloat16, whose partials are
+// fp32) and keeps them in registers, where two units spilled (measured on
+// GB300: 1.1-1.4x faster for fp32 and 1.2-1.8x for bfloat16 at 4-8 ranks x
+// 1 KiB-1 MiB per rank).
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+constexpr int ring_units_per_thread(int dt, int proto) { return proto == kProtoLL ? 1 : kRingUnitsPerThread; }
 // Two-shot: 16-byte units per thread per tile, and the CTAs per SM its
 // kernel is compiled for: two, so that twice the warps hide the loads'
 // latency (on GB300, 2 ranks x 64-256 MiB fp32: one CTA per SM with 4

@@ -60,8 +60,8 @@
  *   RRA_RING_LL_STAGED_MAX_BYTES  on 16-byte aligned buffers with 2 ranks
  *                        or more, chunks up to this many bytes take LL
  *                        lines (measured faster there; default 256 KiB from
- *                        3 ranks and 128 KiB at 2, bfloat16 8 KiB and
- *                        2 KiB), larger ones the staged form
+ *                        3 ranks and 128 KiB at 2, bfloat16 128 KiB),
+ *                        larger ones the staged form
  *   RRA_RING_LL_MAX_BYTES  on other buffers, the largest chunk the per-warp
  *                        ring sends as LL lines (64 KiB; larger: Simple)
  *   RRA_RING_CLUSTER     1: the ring on thread-block clusters
