@@ -13,10 +13,10 @@
 // total travels down unchanged, so every rank holds the same bits.
 //
 // Design on one GPU: one persistent cooperative launch of n x C CTAs of 8
-// warps.  A warp tile is 32 lanes x 2 units; warp w of CTA (r, ch) takes
-// tiles ch*8 + w, + 8C, ... of both parts, as does the same warp of every
-// other rank, so each edge of a tile joins two warps that handle it in the
-// same order.  Per tile:
+// warps.  A warp tile is 32 lanes x kTreeLLUnits units (one unit a lane);
+// warp w of CTA (r, ch) takes tiles ch*8 + w, + 8C, ... of both parts, as
+// does the same warp of every other rank, so each edge of a tile joins two
+// warps that handle it in the same order.  Per tile:
 //   up    acc = x; for each child, poll its up lines of the tile and add
 //         them (accumulator words: bfloat16 partials travel as float32);
 //         below the root, post acc as LL lines in the own up region; at the

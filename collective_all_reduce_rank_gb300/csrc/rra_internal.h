@@ -288,9 +288,13 @@ cudaError_t ring_staged_occupancy(int dt, int tile_units, int stages, int* max_b
 cudaError_t launch_ring_staged(int dt, const RingArgs& a, int grid, cudaStream_t s);
 
 // LL tree: 16-byte aligned buffers; kTreeLLThreads threads, each lane
-// kTreeLLUnits units per tile.
+// kTreeLLUnits units per tile.  One unit a lane: more warps share a message
+// and fewer polled lines sit in each lane (measured on GB300 against two:
+// 1.1-1.4x faster for fp32 and bfloat16 from 16 KiB to 256 KiB per rank at
+// 2-8 ranks; 0.88-0.97x for bfloat16 at 8 ranks x 512 KiB-1 MiB and 2
+// ranks x 1 MiB).
 constexpr int kTreeLLThreads = 256;
-constexpr int kTreeLLUnits = 2;
+constexpr int kTreeLLUnits = 1;
 cudaError_t tree_ll_occupancy(int dt, int* max_blocks_per_sm);
 cudaError_t launch_tree_ll(int dt, const TreeLLArgs& a, int grid, cudaStream_t s);
 
