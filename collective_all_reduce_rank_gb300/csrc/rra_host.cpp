@@ -547,16 +547,16 @@ rra_status_t run_tree_ll(DevState* s, const void* const* in, void* const* out, i
 // The tree's form: RRA_TREE_PROTO=ll | staged forces one; by default LL
 // lines for messages up to tree_ll_max_bytes per rank whose lines fit the
 // LL region, the staged tree above.  Measured on GB300 (CUDA graph of 50
-// calls, microseconds per call, LL against staged): fp32 at 8 ranks 6.3
-// against 18.6 at 1 KiB per rank, 11.5 against 26.6 at 256 KiB, 13.5
-// against 30.7 at 512 KiB; at 2 ranks 4.0 against 7.0 at 1 KiB, 9.9
-// against 13.4 at 2 MiB; bf16 at 8 ranks 6.9 against 18.9 at 1 KiB, 19.7
-// against 31.0 at 512 KiB; at 2 ranks 7.7 against 11.2 at 1 MiB and 13.9
-// against 13.6 at 2 MiB; with the 64 MiB region, up to the largest
-// messages whose lines fit, fp32 at 2 ranks x 8 MiB 27.4 against 32.7, at
-// 4 x 4 MiB 30.3 against 48.2, at 8 x 2 MiB 27.4 against 56.1, bf16 at 4
-// ranks x 2 MiB 23.1 against 29.5.  So LL wherever its lines fit, but for
-// bf16 at 2 ranks above 1 MiB per rank.
+// calls, microseconds per call, LL against staged): fp32 at 8 ranks 7.4
+// against 20.6 at 1 KiB per rank, 9.3 against 26.7 at 256 KiB, 11.6
+// against 30.7 at 512 KiB; at 2 ranks 4.3 against 8.1 at 1 KiB, 10.2
+// against 13.3 at 2 MiB; bf16 at 8 ranks 8.3 against 20.6 at 1 KiB, 22.0
+// against 30.9 at 512 KiB; at 2 ranks 9.5 against 11.3 at 1 MiB and 15.1
+// against 13.5 at 2 MiB; with the 64 MiB region, up to the largest
+// messages whose lines fit, fp32 at 2 ranks x 8 MiB 26.8 against 32.8, at
+// 4 x 4 MiB 26.4 against 48.2, at 8 x 2 MiB 24.1 against 55.8, bf16 at 4
+// ranks x 2 MiB 30.6 against 29.5 (within the run-to-run spread).  So LL
+// wherever its lines fit, but for bf16 at 2 ranks above 1 MiB per rank.
 size_t tree_ll_max_bytes(int n, rra_dtype_t dt);
 
 rra_status_t run_tree(DevState* s, const void* const* in, void* const* out, int n, size_t count, rra_dtype_t dt,
