@@ -21,8 +21,9 @@
 // the rest of its line.
 //
 // Throughput: LL pack gives every thread one group of lines over a grid that
-// covers the payload, LL128 pack one quad per warp per trip; the unpack kernels
-// keep several groups of every source in flight per thread.  Partial groups
+// covers the payload, LL128 pack eight quads per warp per trip (over a grid
+// that covers the payload from 64 MiB); the unpack kernels keep several
+// groups of every source in flight per thread, on a resident grid.  Partial groups
 // and polling take out-of-line paths, so the fast paths stay lean.
 #include "common.cuh"
 
@@ -282,7 +283,6 @@ static __device__ __noinline__ void ll128_pack_slow(const LLArgs& a, size_t j, i
   st_volatile(static_cast<char*>(a.wire_out) + 128 * j + 16 * li, make_uint4(w0, w1, w2, w3));
 }
 
-constexpr int kL128PackBatch = 8;  // quads per warp per trip, loads all in flight before the stores
 
 // kL128PackBatch quads per warp per trip of a grid-stride loop; whole quads
 // of an aligned payload read their 120-byte line bodies with 8-byte loads

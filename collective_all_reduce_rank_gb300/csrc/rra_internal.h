@@ -226,6 +226,8 @@ constexpr int twoshot_tile_units(int n) {
   return twoshot_split(n) ? kDirectThreads / 2 : kDirectThreads * twoshot_units_per_thread(n);
 }
 constexpr int kLLThreads = 256;
+// LL128 pack: quads per warp per trip, every load in flight before the stores
+constexpr int kL128PackBatch = 8;
 
 // SM budget set by rra_set_max_ctas (0: none); kernels_direct.cu caps its
 // grids with it.

@@ -52,6 +52,18 @@ def test_pack_bytes_match_oracle(fmt, B):
     assert wire.cpu().numpy().tobytes() == want.tobytes()
 
 
+@pytest.mark.parametrize("B", [(64 << 20) - 480, 64 << 20, (64 << 20) + 484, (100 << 20) + 6])
+def test_ll128_pack_large_payloads(B):
+    # from 64 MiB the LL128 pack runs on a grid covering the payload (eight
+    # quads a warp in one trip), below it on a resident grid-stride grid
+    pack, _, wire_bytes, opack, _ = FMT["ll128"]
+    payload = np.random.default_rng(B).integers(0, 256, size=B, dtype=np.uint8)
+    wire = _wire_buf(wire_bytes(B))
+    pack(_dev_bytes(payload), wire, 0x0F0E0D0C0B0A0908)
+    assert rra.rra_query_status()[0] == 0
+    assert wire.cpu().numpy().tobytes() == opack(payload, 0x0F0E0D0C0B0A0908).tobytes()
+
+
 @pytest.mark.parametrize("fmt", list(FMT))
 def test_pack_unaligned_payload(fmt):
     import torch
