@@ -957,6 +957,99 @@ def run_ll_sweep(args):
 
 
 # --------------------------------------------------------------------------
+# one-shot / direct reduce-scatter / direct all-gather: resident against
+# covering grid
+# --------------------------------------------------------------------------
+DIRECT_SIZES = tuple(4 << (20 + 2 * k) for k in range(5))  # 4 MiB .. 1 GiB per rank, x4
+
+
+def run_direct_sweep(args):
+    """One-shot all-reduce, direct reduce-scatter and direct all-gather of
+    n = 2, 4, 8 ranks x 4 MiB .. 1 GiB per rank (float32, bfloat16; the
+    sweep's seeded recipe), each timed with RRA_DIRECT_GRID=resident and
+    with the library's default grid choice (covering from its thresholds).
+    The two forms' outputs are compared bit for bit at every point (parity
+    with the oracle is the tests' job)."""
+    import torch
+
+    import collective_all_reduce_rank_gb300 as rra
+    from collective_all_reduce_rank_gb300 import inputs
+
+    torch.cuda.set_device(0)
+    rra.rra_init(0)
+    stream = torch.cuda.Stream()
+    peak, _ = peaks()
+    out = open(args.direct_sweep, "w")
+    codes = {"float32": (rra.RRA_FLOAT32, 4), "bfloat16": (rra.RRA_BFLOAT16, 2)}
+
+    def last_grid():
+        return int(rra.rra_dump_recent().strip().splitlines()[-1].split("grid=")[1].split()[0])
+
+    try:
+        for dtype, (code, e) in codes.items():
+            for n in (2, 4, 8):
+                for S in DIRECT_SIZES:
+                    count = S // e
+                    rc = count // n
+                    xs = inputs.cfg_sweep(n, S, dtype, seed=S + n)
+                    if dtype == "bfloat16":
+                        ins = [torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16) for x in xs]
+                    else:
+                        ins = [torch.from_numpy(x).cuda() for x in xs]
+                    del xs
+                    ar = [torch.empty_like(t) for t in ins]
+                    rs = [torch.empty(rc, dtype=ins[0].dtype, device="cuda") for _ in range(n)]
+                    ag = [torch.empty_like(t) for t in ins]
+                    ops = (
+                        ("one_shot", 2 * n * S,
+                         lambda: rra.rra_allreduce(ins, ar, count, code, rra.RRA_SUM, rra.RRA_ALGO_ONE_SHOT, stream),
+                         ar),
+                        ("rs_direct", (n + 1) * S,
+                         lambda: rra.rra_reduce_scatter(ins, rs, rc, code, rra.RRA_SUM, rra.RRA_ALGO_DIRECT, stream),
+                         rs),
+                        ("ag_direct", (n + 1) * S,
+                         lambda: rra.rra_all_gather(rs, ag, rc, code, rra.RRA_ALGO_DIRECT, stream), ag),
+                    )
+                    for op, fb, call, outs in ops:
+                        res = {}
+                        for form in ("resident", "default"):
+                            if form == "resident":
+                                os.environ["RRA_DIRECT_GRID"] = "resident"
+                            else:
+                                os.environ.pop("RRA_DIRECT_GRID", None)
+                            with torch.cuda.stream(stream):
+                                call()
+                            torch.cuda.synchronize()
+                            grid = last_grid()
+                            kept = [t.clone() for t in outs]
+                            us, p10, p90 = time_call(torch, call, stream, fb)
+                            res[form] = (us, p10, p90, grid, kept)
+                        same = all(torch.equal(a.view(torch.int16), b.view(torch.int16))
+                                   for a, b in zip(res["resident"][4], res["default"][4]))
+                        if not same:
+                            raise SystemExit("grid forms differ: %s %s n=%d S=%d" % (op, dtype, n, S))
+                        st, info = rra.rra_query_status(stream)
+                        if st != 0:
+                            raise SystemExit("device status %d %s at %s %s n=%d S=%d" % (st, info, op, dtype, n, S))
+                        for form in ("resident", "default"):
+                            us, p10, p90, grid, _ = res[form]
+                            gbs = fb / (us / 1e6) / 1e9
+                            row = {"op": op, "form": form, "dtype": dtype, "n": n, "bytes_per_rank": S,
+                                   "grid": grid, "us": round(us, 3), "us_p10": round(p10, 3),
+                                   "us_p90": round(p90, 3), "floor_bytes": fb, "GBps": round(gbs, 1),
+                                   "frac_of_measured": round(gbs / peak, 3)}
+                            out.write(json.dumps(row) + "\n")
+                            out.flush()
+                            print(json.dumps(row), flush=True)
+                        del res
+                    del ins, ar, rs, ag
+                    torch.cuda.empty_cache()
+    finally:
+        os.environ.pop("RRA_DIRECT_GRID", None)
+    out.close()
+
+
+# --------------------------------------------------------------------------
 # message-size sweep (config 5) and the selector table
 # --------------------------------------------------------------------------
 SWEEP_DTYPES = ("int32", "bfloat16", "float32")
@@ -1215,6 +1308,8 @@ def main():
     ap.add_argument("--ll-sweep", default=None,
                     help="write the LL / LL128 payload sweep (1 KiB .. 256 MiB, 4 sources) to this JSONL file")
     ap.add_argument("--sweep", default=None, help="write the message-size sweep to this JSONL file")
+    ap.add_argument("--direct-sweep", default=None,
+                    help="write one-shot / direct RS / direct AG on resident and default grids to this JSONL file")
     ap.add_argument("--sweep-max", type=int, default=1 << 30)
     ap.add_argument("--sweep-cold", action="store_true",
                     help="flush L2 (write twice its size) before every timed call of the sweep")
@@ -1229,6 +1324,8 @@ def main():
         run_sweep(args)
     elif args.ll_sweep:
         run_ll_sweep(args)
+    elif args.direct_sweep:
+        run_direct_sweep(args)
     elif args.ring_forms:
         run_ring_forms(args)
     else:

@@ -16,6 +16,8 @@
 // (same page, "Algorithms": reduce your 1/n slice, then read the sums
 // back), exposed on their own.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
 #include "common.cuh"
 
@@ -144,7 +146,8 @@ __global__ void __launch_bounds__(kDirectThreads) direct_ag_kernel(const __grid_
 // 0.94-0.99 -> 0.98-1.05, direct all-gather 0.77-0.90 -> 0.86-1.03.  Below
 // the thresholds (256 MB of floor bytes for one-shot, 64 MB for the
 // reduce-scatter and all-gather) the resident grid measured as fast or up
-// to 13% faster.  An SM budget (rra_set_max_ctas) keeps the resident grid.
+// to 13% faster.  An SM budget (rra_set_max_ctas) keeps the resident grid;
+// RRA_DIRECT_GRID=resident | cover forces one form at every size.
 // ---------------------------------------------------------------------------
 static int device_sms() {
   int dev = 0, sms = 0;
@@ -160,12 +163,22 @@ static int occupancy_of(Kern k) {
   return b;
 }
 
+// RRA_DIRECT_GRID, read at every call: 0 by size, 1 resident, 2 cover
+static int forced_grid() {
+  const char* e = std::getenv("RRA_DIRECT_GRID");
+  if (!e) return 0;
+  if (!std::strcmp(e, "resident")) return 1;
+  if (!std::strcmp(e, "cover")) return 2;
+  return 0;
+}
+
 static int grid_for(size_t units, int occ, int rows, int upt, size_t floor_bytes, size_t cover_from) {
   const size_t want = (units + kDirectThreads - 1) / kDirectThreads;
   int per_row = std::max(1, device_sms() * occ / rows);
+  const int forced = forced_grid();
   if (max_ctas_cap() > 0) {
     per_row = std::max(1, std::min(per_row, max_ctas_cap() / rows));
-  } else if (floor_bytes >= cover_from) {
+  } else if (forced == 2 || (forced == 0 && floor_bytes >= cover_from)) {
     const size_t cover = (units + (size_t)kDirectThreads * upt - 1) / ((size_t)kDirectThreads * upt);
     return (int)std::max<size_t>(1, std::min<size_t>(cover, 0x7fffffff));
   }

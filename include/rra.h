@@ -91,6 +91,12 @@
  *   RRA_ONESHOT_PER_RANK 1: one-shot reads the n inputs once per rank, as
  *                        n GPUs would (out of place only; in place keeps
  *                        the combined form)
+ *   RRA_DIRECT_GRID      grid of one-shot and the direct reduce-scatter and
+ *                        all-gather: resident (SMs x occupancy, grid-stride)
+ *                        or cover (one trip a thread); default: cover from
+ *                        256 MB of floor bytes (one-shot) or 64 MB (the
+ *                        others), resident below.  An SM budget keeps the
+ *                        resident grid.
  */
 #ifndef RRA_H
 #define RRA_H
