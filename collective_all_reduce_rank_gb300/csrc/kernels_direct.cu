@@ -23,18 +23,21 @@
 
 namespace rra {
 
-// Up to four ranks a thread takes two units per trip (2n loads in flight);
-// from five the kernel is built for two CTAs per SM with one unit per trip
-// (n loads a thread, 53-60 registers at eight ranks against 94): on GB300 at
-// 8 ranks x 8 MiB fp32 0.85 -> 0.90 of the HBM copy rate, bf16 at 64-256
-// MiB 0.88-0.92 -> 0.90-0.93, fp32 at 64-256 MiB within 0.5%.
-template <int N>
+// Up to four ranks (three for bfloat16) a thread takes two units per trip
+// (2n loads in flight); above, the kernel is built for two CTAs per SM with
+// one unit per trip (n loads a thread, 53-60 registers at eight ranks
+// against 94): on GB300 at 8 ranks x 8 MiB fp32 0.85 -> 0.90 of the HBM
+// copy rate, bf16 at 64-256 MiB 0.88-0.92 -> 0.90-0.93, fp32 at 64-256 MiB
+// within 0.5%.  bfloat16 at four ranks (78 registers with two units, one
+// CTA per SM; 44 with one): 16 MiB-1 GiB 0.89-0.99 -> 0.95-1.05; at two
+// and three ranks one unit measured 3-13% slower.
+template <int N, int DT>
 __host__ __device__ constexpr bool oneshot_two_units() {
-  return N <= 4;
+  return DT == RRA_BFLOAT16 ? N <= 3 : N <= 4;
 }
 
 template <int N, int DT, bool VEC>
-__global__ void __launch_bounds__(kDirectThreads, oneshot_two_units<N>() ? 1 : 2)
+__global__ void __launch_bounds__(kDirectThreads, oneshot_two_units<N, DT>() ? 1 : 2)
     oneshot_kernel(const __grid_constant__ DirectArgs a) {
   const size_t count = a.count;
   const size_t units = (count + Elem<DT>::kPerUnit - 1) / Elem<DT>::kPerUnit;
@@ -46,7 +49,7 @@ __global__ void __launch_bounds__(kDirectThreads, oneshot_two_units<N>() ? 1 : 2
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   // two units per trip: 2N independent 16-byte loads in flight per thread
-  for (; oneshot_two_units<N>() && u + stride < units; u += 2 * stride) {
+  for (; oneshot_two_units<N, DT>() && u + stride < units; u += 2 * stride) {
     const size_t u1 = u + stride;
     const int v0 = unit_valid<DT>(u, count), v1 = unit_valid<DT>(u1, count);
     uint4 x0[N], x1[N];
@@ -222,11 +225,12 @@ static int grid_for(size_t units, int occ, int rows, int upt, size_t floor_bytes
   }
 
 // Per kernel: units a thread takes in one trip (one-shot two up to four
-// ranks, the reduce-scatter one, the all-gather two); floor bytes per unit
+// ranks, three for bfloat16; the reduce-scatter one, the all-gather two);
+// floor bytes per unit
 // of `units` (one-shot: n reads and n writes of each unit; reduce-scatter
 // and all-gather, `units` being one rank's slice: (n + 1) n bytes of each);
 // the floor bytes from which the grid covers.
-RRA_DIRECT_DISPATCH(oneshot_kernel, (oneshot_two_units<N>() ? 2 : 1), 2 * N * 16, (size_t)256 << 20)
+RRA_DIRECT_DISPATCH(oneshot_kernel, (oneshot_two_units<N, DT>() ? 2 : 1), 2 * N * 16, (size_t)256 << 20)
 RRA_DIRECT_DISPATCH(direct_rs_kernel, 1, (N + 1) * N * 16, (size_t)64 << 20)
 RRA_DIRECT_DISPATCH(direct_ag_kernel, 2, (N + 1) * N * 16, (size_t)64 << 20)
 

@@ -58,12 +58,12 @@ def _count_for(units, e, ragged):
 
 
 @pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
-@pytest.mark.parametrize("n", [2, 8])
+@pytest.mark.parametrize("n", [2, 4, 8])
 def test_oneshot_either_side(dtype, n):
     g = G()
     e = ES[dtype]
     t = _units_from(ONESHOT_FROM, 2 * n * 16)
-    upt = 2 if n <= 4 else 1
+    upt = 2 if n <= (3 if dtype == "bfloat16" else 4) else 1  # units a thread takes in one trip
     grids = []
     for units, ragged in ((t - 1, False), (t + 1, True)):
         count = _count_for(units, e, ragged)
