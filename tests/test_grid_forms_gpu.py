@@ -110,3 +110,37 @@ def test_direct_rs_ag_either_side(dtype, n):
     for grids in (rs_grids, ag_grids):
         (below, below_cover), (above, above_cover) = grids
         assert below != below_cover and above == above_cover, grids
+
+
+@pytest.mark.parametrize("form", ["resident", "cover"])
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+@pytest.mark.parametrize("n,rc", [(3, 100_003), (5, 4_097), (8, 1)])
+def test_forced_grid_forms_match_oracle(form, dtype, n, rc, monkeypatch):
+    # RRA_DIRECT_GRID forces one grid at every size: small and ragged
+    # messages on the covering grid, and the resident one, give the
+    # oracle's bits for all three operations
+    g = G()
+    monkeypatch.setenv("RRA_DIRECT_GRID", form)
+    dist = "int20" if dtype == "int32" else "normal"
+    xs = inputs.make_ranks(n, n * rc, dtype, dist, seed=rc + n)
+    ins = [g.to_dev(x, dtype) for x in xs]
+    outs = g.empty(n, n * rc, dtype)
+    rra.rra_allreduce(ins, outs, n * rc, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_ONE_SHOT)
+    _last_grid()
+    want, _, _ = oracle.allreduce("oneshot", xs, dtype)
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "one-shot %s r=%d" % (form, r))
+    outs = g.empty(n, rc, dtype)
+    rra.rra_reduce_scatter(ins, outs, rc, g.CODE[dtype], rra.RRA_SUM, rra.RRA_ALGO_DIRECT)
+    _last_grid()
+    want, _, _ = oracle.reduce_scatter("direct", xs, dtype)
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "rs %s r=%d" % (form, r))
+    shards = [np.ascontiguousarray(x[:rc]) for x in xs]
+    ins = [g.to_dev(x, dtype) for x in shards]
+    outs = g.empty(n, n * rc, dtype)
+    rra.rra_all_gather(ins, outs, rc, g.CODE[dtype], rra.RRA_ALGO_DIRECT)
+    _last_grid()
+    want, _, _ = oracle.all_gather("direct", shards, dtype)
+    for r in range(n):
+        g.assert_bits_equal(g.to_host(outs[r], dtype), want[r], "ag %s r=%d" % (form, r))
