@@ -129,3 +129,13 @@ def test_dominant_kernel_sums_its_operations():
     # a kernel launched four times by one operation can dominate too
     t.update(ll_pack=2.0)
     assert bench.dominant(ops, t)[:3] == ("ll_pack_kernel", "ll_pack", 100)
+
+
+def test_traffic_capture_matches_the_kernel_source():
+    # the bench line's DRAM traffic comes from a committed ncu capture; it
+    # must have been taken on the kernel source as it stands (bench.py
+    # reports null otherwise)
+    import bench
+
+    t = bench.load_traffic("ar_ring")
+    assert t is not None and t > 0
